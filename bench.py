@@ -1,0 +1,465 @@
+"""Benchmark of the MoE dispatch/combine hot path on GB300.
+
+One step = layout (ep_get_dispatch_layout) + dispatch (ep_dispatch) + combine
+(ep_combine) over one batch of the DeepSeek-V3-shaped prefill workload
+(T=4096 tokens, H=7168 bf16, E=256 experts, top-8), inputs resident in HBM.
+The headline runs on all SMs; the same step is also timed with a 24-SM
+budget. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (torchrun): every rank runs an independent replica on its own GPU
+(the path has no exchange step on one GPU: replicas only); value = tokens
+of all ranks / max-over-ranks time.
+--impl reference: the CPU oracle (single thread) on a bounded sample of the
+same workload, timed as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_movement_gb300 import workloads as W  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s and HBM GB/s (% of GB300 peak) at 24 SMs / all SMs"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------
+# bytes the method must move (per launch)
+
+def algorithmic_bytes(T: int, H: int, K: int, E: int, R: int) -> dict:
+    row = 2 * H
+    return {
+        "layout": 8 * T * K + 4 * T * K + 4 * E + 4 * (E + 1),
+        "dispatch": T * row + R * row + 4 * T * K,
+        "combine": R * row + 4 * T * K + 4 * T * K + T * row,
+    }
+
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: torch copy_, read+write bytes)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, or None if absent
+    or taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+        src = os.path.join(ROOT, "combine_movement_gb300", "csrc", rec["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if h != rec["source_sha256"]:
+            return None
+        return int(rec["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the step
+
+class Step:
+    """Device buffers of one workload and the three calls of one step."""
+
+    def __init__(self, ep, inp: W.Inputs, dev: torch.device):
+        wl = inp.wl
+        self.ep, self.wl, self.dev = ep, wl, dev
+        self.T, self.H, self.E, self.K = wl.T, wl.H, wl.E, wl.K
+        self.R = wl.T * wl.K
+        self.idx = inp.topk_idx.to(dev)
+        self.w = inp.topk_w.to(dev)
+        self.x = inp.x.to(dev)
+        self.counts = torch.empty(self.E, dtype=torch.int32, device=dev)
+        self.offsets = torch.empty(self.E + 1, dtype=torch.int32, device=dev)
+        self.slot = torch.empty((self.T, self.K), dtype=torch.int32, device=dev)
+        nws = ep.ep_layout_workspace_bytes(self.T, self.K, self.E)
+        self.ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+        self.layout_launches = 3 if nws else 1
+        self.recv_x = torch.empty((self.R, self.H), dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # the experts between dispatch and combine are a fixed stand-in
+        self.layout()
+        self.dispatch()
+        self.expert_out = W.expert_standin(self.recv_x, wl.expert_scale)
+        torch.cuda.synchronize(dev)
+
+    def layout(self, stream=None):
+        self.ep.ep_get_dispatch_layout(self.idx, self.E, self.counts, self.offsets, self.slot,
+                                       self.ws, self.status, stream)
+
+    def dispatch(self, stream=None):
+        self.ep.ep_dispatch(self.x, self.slot, self.recv_x, None, None, None, self.status, stream)
+
+    def combine(self, stream=None):
+        self.ep.ep_combine(self.expert_out, self.slot, self.w, self.y, self.status, stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        return self.layout_launches + 2
+
+
+def barrier(dist_on: bool):
+    if dist_on:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, dist_on: bool) -> float:
+    if not dist_on:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch.cuda.Stream,
+               sampler_index: int = -1) -> dict:
+    """W untimed steps, then exactly K steps between barrier+synchronize,
+    with per-kernel CUDA events recorded on the launching stream."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step.layout(stream)
+            step.dispatch(stream)
+            step.combine(stream)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(dist_on)
+        sampler = ClockSampler(sampler_index) if sampler_index >= 0 else None
+        if sampler:
+            sampler.__enter__()
+        start.record(stream)
+        for i in range(steps):
+            e = ev[i]
+            e[0].record(stream)
+            step.layout(stream)
+            e[1].record(stream)
+            step.dispatch(stream)
+            e[2].record(stream)
+            step.combine(stream)
+            e[3].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.__exit__(None, None, None)
+        barrier(dist_on)
+    total_ms = start.elapsed_time(end)
+    lay = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
+    dis = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
+    com = [ev[i][2].elapsed_time(ev[i][3]) for i in range(steps)]
+    return {"total_ms": total_ms, "layout_ms": lay, "dispatch_ms": dis, "combine_ms": com,
+            "clocks": sampler.summary() if sampler else None}
+
+
+def time_e2e(step: Step, inp: W.Inputs, steps: int, warmup: int, stream) -> dict:
+    """Same step through the public API with host-resident inputs: every step
+    copies x, topk_idx and topk_w from pinned host memory to the device and
+    reads y back, inside the timed region."""
+    hx = inp.x.pin_memory()
+    hidx = inp.topk_idx.pin_memory()
+    hw = inp.topk_w.pin_memory()
+    hy = torch.empty_like(step.y, device="cpu").pin_memory()
+    h2d = hx.numel() * hx.element_size() + hidx.numel() * 8 + hw.numel() * 4
+    d2h = hy.numel() * hy.element_size()
+
+    def one():
+        step.x.copy_(hx, non_blocking=True)
+        step.idx.copy_(hidx, non_blocking=True)
+        step.w.copy_(hw, non_blocking=True)
+        step.layout(stream)
+        step.dispatch(stream)
+        step.combine(stream)
+        hy.copy_(step.y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            one()
+        e.record(stream)
+        torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"ms_per_step": ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and reference arm)
+
+def oracle_sample(inp: W.Inputs, tokens: int):
+    """Run the oracle's layout -> dispatch -> combine on the first `tokens`
+    tokens of the workload; returns seconds."""
+    import oracle
+    o = oracle.Oracle()
+    idx = np.ascontiguousarray(inp.topk_idx.numpy()[:tokens])
+    xb = np.ascontiguousarray(inp.x_bits()[:tokens])
+    w = np.ascontiguousarray(inp.topk_w.numpy()[:tokens])
+    t0 = time.perf_counter()
+    _, offsets, slot, _ = o.layout(idx, inp.wl.E)
+    recv, _, _ = o.dispatch(xb, slot, int(offsets[-1]))
+    o.combine(recv, slot, w)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp: W.Inputs, budget_s: float = 10.0) -> dict:
+    tokens = min(inp.wl.T, 1024)
+    done, spent = 0, 0.0
+    while spent < budget_s and done < 64:
+        spent += oracle_sample(inp, tokens)
+        done += 1
+    return {"value": tokens * done / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {tokens} tokens of {inp.wl.name} (layout+dispatch+combine, "
+                      f"identity experts), {done} repetitions, {spent:.1f} s single-threaded"}
+
+
+def run_reference(args, wl: W.Workload, rank: int) -> None:
+    if rank != 0:
+        return
+    inp = W.make_inputs(wl)
+    tokens = min(wl.T, 256)
+    for _ in range(args.warmup):
+        oracle_sample(inp, tokens)
+    secs = [oracle_sample(inp, tokens) for _ in range(args.steps)]
+    total = sum(secs)
+    value = tokens * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl_desc(wl), "sample_tokens": tokens},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {tokens} of {wl.T} tokens per step, single-threaded C oracle"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def wl_desc(wl: W.Workload) -> str:
+    return (f"{wl.name}: T={wl.T} H={wl.H} bf16 E={wl.E} top-{wl.K} {wl.routing} routing, "
+            f"expert stand-in x{wl.expert_scale}")
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="deepseek-v3-prefill", choices=sorted(W.BY_NAME))
+    ap.add_argument("--budget-sms", type=int, default=24, help="second SM budget to report")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    if dist_on:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    wl = W.BY_NAME[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+        if dist_on:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from combine_movement_gb300 import ep
+
+    inp = W.make_inputs(wl)
+    step = Step(ep, inp, dev)
+    stream = torch.cuda.Stream(dev)
+    sms_all = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    ep.ep_set_num_sms(0)
+    main_run = time_steps(step, args.steps, args.warmup, dist_on, stream, sampler_index=local)
+    ep.ep_set_num_sms(args.budget_sms)
+    budget_run = time_steps(step, args.steps, args.warmup, dist_on, stream)
+    ep.ep_set_num_sms(0)
+    e2e = time_e2e(step, inp, max(3, args.steps // 2), 3, stream)
+    st = ep.ep_get_status(step.status)
+    if st != 0:
+        raise SystemExit(f"device status {st}: {ep.ep_status_string(st)}")
+
+    ab = algorithmic_bytes(step.T, step.H, step.K, step.E, step.R)
+    peak, peak_src = peak_hbm()
+
+    def summarize(run: dict, nsms: int) -> dict:
+        ms = max_over_ranks(run["total_ms"] / args.steps, dist_on)
+        d = statistics.mean(run["dispatch_ms"])
+        c = statistics.mean(run["combine_ms"])
+        lay = statistics.mean(run["layout_ms"])
+        moved = ab["dispatch"] + ab["combine"]
+        return {
+            "num_sms": nsms, "ms_per_step": ms,
+            "tokens_per_s": world * step.T / (ms * 1e-3),
+            "dispatch_combine_gbs": moved / ((d + c) * 1e-3) / 1e9,
+            "dispatch_combine_frac": moved / ((d + c) * 1e-3) / 1e9 / peak,
+            "dispatch_us": 1e3 * d, "combine_us": 1e3 * c, "layout_us": 1e3 * lay,
+            "dispatch_gbs": ab["dispatch"] / (d * 1e-3) / 1e9,
+            "combine_gbs": ab["combine"] / (c * 1e-3) / 1e9,
+        }
+
+    s_all = summarize(main_run, sms_all)
+    s_bud = summarize(budget_run, min(args.budget_sms, sms_all))
+    dom = "dispatch" if s_all["dispatch_us"] >= s_all["combine_us"] else "combine"
+    achieved = s_all[f"{dom}_gbs"]
+    traffic = kernel_traffic(dom)
+    e2e_ms = max_over_ranks(e2e["ms_per_step"], dist_on)
+
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline else cpu_baseline(inp)
+        line = {
+            "metric": METRIC,
+            "value": s_all["tokens_per_s"],
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": s_all["ms_per_step"],
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {
+                "workload": wl_desc(wl),
+                "num_sms": sms_all,
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                "accumulate": "fp32 (combine)",
+                "l2": "no flush: inputs larger than L2 (x 58.7 MB is re-read after "
+                      "~1 GB of other traffic per step; recv/expert_out 470 MB each)",
+            },
+            "hbm": {
+                "all_sms": s_all,
+                f"sms_{args.budget_sms}": s_bud,
+                "peak_gbs": peak,
+                "peak_source": peak_src,
+                "algorithmic_bytes_per_step": ab,
+            },
+            "roofline": {
+                "bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                "algorithmic_bytes": ab[dom],
+            },
+            "e2e": {
+                "value": world * step.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+            },
+            "gpu_launches": step.launches_per_step * args.steps,
+            "clocks": main_run["clocks"],
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

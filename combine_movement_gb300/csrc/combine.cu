@@ -1,0 +1,164 @@
+// combine.cu -- gather every token's K expert rows back into token order and
+// reduce them with the routing weights.
+//
+// The pages describe only DeepEP's dispatch ("How DeepEP Utilizes TMA
+// Instructions for Minimal SM Usage on Hopper GPUs"); combine is its inverse
+// in the MoE layer the page is about: y[t] = sum_k w[t,k] * expert_out[slot[t,k]].
+// The arithmetic is fixed so the result is unique: fp32 accumulator starting
+// at +0.0f, one fused multiply-add per k in ascending k (entries with slot < 0
+// skipped), one bf16 round-to-nearest-even per output element.
+//
+// Mapping: persistent grid of one CTA per SM (the SM budget). A unit is one
+// 512-byte column block of one token row (32 lanes x 16 bytes); every warp
+// takes a contiguous, equal range of units, so the load is balanced to within
+// one unit whatever T and the budget. For each token the warp reads slot and
+// weight once (lanes k < K) and broadcasts them with warp shuffles; each lane
+// then issues K independent 16-byte loads (read-only path, no L1 allocation),
+// widens bf16 to fp32 exactly (bit shift), runs the fma chain in k order and
+// writes 16 bytes, so every warp store is a coalesced 512-byte row segment.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ep.h"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace ep {
+namespace {
+
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+constexpr int kCombineThreads = 512;
+constexpr uint32_t kColBytes = 512;  // row bytes one warp covers per unit
+
+__device__ __forceinline__ uint4 ld_expert(const uint8_t* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// acc[i] = fma(w, float(bf16 element i of v), acc[i]) for the 8 elements of v.
+__device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4& v) {
+    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(w, __uint_as_float(q[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 round8(const float (&acc)[8]) {
+    return make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+}
+
+// KT > 0: K == KT known at compile time (slots, row pointers and weights in
+// registers). KT == 0: any K <= 32, broadcast per unit.
+template <int KT>
+__global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const CombineArgs a) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int64_t n_cb = (a.row_bytes + kColBytes - 1) / kColBytes;
+    const int64_t units = a.T * n_cb;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
+    const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
+    const int64_t u0 = units * gw / nw_total;
+    const int64_t u1 = units * (gw + 1) / nw_total;
+    const int K = KT > 0 ? KT : a.K;
+    constexpr int KR = KT > 0 ? KT : 1;
+
+    int64_t tok = -1;
+    const uint8_t* rowp[KR];
+    float wk[KR];
+    bool on[KR];
+    int32_t s_lane = -1;
+    float w_lane = 0.0f;
+
+    for (int64_t u = u0; u < u1; ++u) {
+        const int64_t t = u / n_cb;
+        const uint32_t col = static_cast<uint32_t>(u - t * n_cb) * kColBytes + lane * 16u;
+        if (t != tok) {
+            tok = t;
+            int32_t s = lane < K ? __ldg(a.slot + t * K + lane) : -1;
+            const float w = lane < K ? __ldg(a.topk_w + t * K + lane) : 0.0f;
+            if (s >= a.num_recv) {
+                set_status(a.status, EP_ERR_BAD_SLOT);
+                s = -1;
+            }
+            s_lane = s;
+            w_lane = w;
+            if (KT > 0) {
+#pragma unroll
+                for (int k = 0; k < KR; ++k) {
+                    const int32_t sk = __shfl_sync(kFullMask, s, k);
+                    wk[k] = __shfl_sync(kFullMask, w, k);
+                    on[k] = sk >= 0;
+                    rowp[k] = a.expert_out + static_cast<int64_t>(sk < 0 ? 0 : sk) * a.row_bytes;
+                }
+            }
+        }
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        const bool in_row = col < a.row_bytes;
+        if (KT > 0) {
+            uint4 v[KR];
+#pragma unroll
+            for (int k = 0; k < KR; ++k) v[k] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int k = 0; k < KR; ++k)
+                if (on[k] && in_row) v[k] = ld_expert(rowp[k] + col);
+#pragma unroll
+            for (int k = 0; k < KR; ++k)
+                if (on[k] && in_row) fma8(acc, wk[k], v[k]);
+        } else {
+            for (int k = 0; k < K; ++k) {
+                const int32_t sk = __shfl_sync(kFullMask, s_lane, k);
+                const float w = __shfl_sync(kFullMask, w_lane, k);
+                if (sk >= 0 && in_row)
+                    fma8(acc, w, ld_expert(a.expert_out + static_cast<int64_t>(sk) * a.row_bytes + col));
+            }
+        }
+        if (in_row) st_v4(a.y + t * static_cast<int64_t>(a.row_bytes) + col, round8(acc));
+    }
+}
+
+template <int KT>
+cudaError_t launch_k(const CombineArgs& a, int grid, cudaStream_t stream) {
+    auto kern = combine_kernel<KT>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kExclusiveSmem));
+    if (err != cudaSuccess) return err;
+    kern<<<grid, kCombineThreads, kExclusiveSmem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t stream) {
+    const int64_t n_cb = (a.row_bytes + kColBytes - 1) / kColBytes;
+    const int64_t units = a.T * n_cb;
+    const int64_t warps_per_cta = kCombineThreads / 32;
+    const int64_t ctas_needed = (units + warps_per_cta - 1) / warps_per_cta;
+    const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
+    if (grid <= 0) return cudaSuccess;
+    switch (a.K) {
+        case 1: return launch_k<1>(a, grid, stream);
+        case 2: return launch_k<2>(a, grid, stream);
+        case 3: return launch_k<3>(a, grid, stream);
+        case 4: return launch_k<4>(a, grid, stream);
+        case 5: return launch_k<5>(a, grid, stream);
+        case 6: return launch_k<6>(a, grid, stream);
+        case 7: return launch_k<7>(a, grid, stream);
+        case 8: return launch_k<8>(a, grid, stream);
+        default: return launch_k<0>(a, grid, stream);
+    }
+}
+
+}  // namespace ep

@@ -1,0 +1,205 @@
+// ep_api.cu -- the C ABI (include/ep.h): argument checks, the SM budget and
+// kernel launches. No allocation, no synchronisation except ep_get_status.
+//
+// The SM budget follows DeepEP's Buffer.set_num_sms ("How DeepEP Utilizes TMA
+// Instructions for Minimal SM Usage on Hopper GPUs", Minimal SM Occupancy
+// Configuration): a process-wide setting read at every launch. Dispatch and
+// combine launch at most that many CTAs, each requesting more than half of an
+// SM's shared memory, so each CTA has an SM to itself and the grid occupies
+// exactly that many SMs. The shared-memory request itself goes through the
+// max-dynamic-shared-memory function attribute, as DeepEP's
+// SET_SHARED_MEMORY_FOR_TMA does (same page, Dynamic Shared Memory
+// Configuration).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "../../include/ep.h"
+#include "kernels.cuh"
+
+namespace {
+
+std::atomic<int> g_num_sms{0};
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_smem_optin[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// SM count and per-block shared-memory opt-in of the current device (cached).
+bool device_limits(int* sm_count, int* smem_optin) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (dev >= 0 && dev < kMaxDevices) {
+        int c = g_sm_count[dev].load(std::memory_order_relaxed);
+        int s = g_smem_optin[dev].load(std::memory_order_relaxed);
+        if (c > 0 && s > 0) {
+            *sm_count = c;
+            *smem_optin = s;
+            return true;
+        }
+    }
+    int c = 0, s = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&s, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return false;
+    if (dev >= 0 && dev < kMaxDevices) {
+        g_sm_count[dev].store(c, std::memory_order_relaxed);
+        g_smem_optin[dev].store(s, std::memory_order_relaxed);
+    }
+    *sm_count = c;
+    *smem_optin = s;
+    return true;
+}
+
+int sms_in_effect(int sm_count) {
+    const int b = g_num_sms.load(std::memory_order_relaxed);
+    return (b <= 0 || b > sm_count) ? sm_count : b;
+}
+
+ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int ep_set_num_sms(int num_sms) {
+    if (num_sms < 0) return -1;
+    g_num_sms.store(num_sms, std::memory_order_relaxed);
+    return num_sms;
+}
+
+int ep_get_num_sms(void) { return g_num_sms.load(std::memory_order_relaxed); }
+
+int ep_num_sms_in_effect(void) {
+    int c = 0, s = 0;
+    if (!device_limits(&c, &s)) return -1;
+    return sms_in_effect(c);
+}
+
+size_t ep_layout_workspace_bytes(int64_t T, int K, int E) {
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return 0;
+    return ep::plan_layout(T * K, E).workspace_bytes;
+}
+
+ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, int E,
+                                   int32_t* counts, int32_t* offsets, int32_t* slot,
+                                   void* workspace, size_t workspace_bytes, int32_t* status,
+                                   void* stream) {
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1) return EP_ERR_INVALID;
+    if (E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
+    if (T * static_cast<int64_t>(K) >= (int64_t{1} << 31)) return EP_ERR_UNSUPPORTED;
+    if (counts == nullptr || offsets == nullptr) return EP_ERR_INVALID;
+    if (T > 0 && (topk_idx == nullptr || slot == nullptr)) return EP_ERR_INVALID;
+    if (!aligned(topk_idx, 8) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(slot, 4) ||
+        !aligned(status, 4))
+        return EP_ERR_INVALID;
+    const ep::LayoutPlan plan = ep::plan_layout(T * K, E);
+    if (plan.workspace_bytes > 0) {
+        if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return EP_ERR_WORKSPACE;
+        if (!aligned(workspace, 4)) return EP_ERR_INVALID;
+    }
+    return from_cuda(ep::launch_layout(topk_idx, T * K, E, counts, offsets, slot,
+                                       static_cast<int32_t*>(workspace), plan, status,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const int32_t* slot,
+                        const float* topk_w, int64_t num_recv, uint16_t* recv_x, float* recv_w,
+                        int32_t* recv_src, int32_t* status, void* stream) {
+    if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || num_recv < 0)
+        return EP_ERR_INVALID;
+    if (T * static_cast<int64_t>(K) >= (int64_t{1} << 31) || num_recv >= (int64_t{1} << 31) ||
+        H * 2 > 0x7FFFFFF0)
+        return EP_ERR_UNSUPPORTED;
+    if (T == 0) return EP_OK;
+    if (x == nullptr || slot == nullptr || (num_recv > 0 && recv_x == nullptr)) return EP_ERR_INVALID;
+    if (recv_w != nullptr && topk_w == nullptr) return EP_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(slot, 4) || !aligned(topk_w, 4) ||
+        !aligned(recv_w, 4) || !aligned(recv_src, 4) || !aligned(status, 4))
+        return EP_ERR_INVALID;
+    int sm_count = 0, smem_optin = 0;
+    if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
+
+    ep::DispatchArgs a{};
+    a.x = reinterpret_cast<const uint8_t*>(x);
+    a.T = T;
+    a.row_bytes = static_cast<uint32_t>(H * 2);
+    a.K = K;
+    a.slot = slot;
+    a.topk_w = topk_w;
+    a.num_recv = num_recv;
+    a.recv_x = reinterpret_cast<uint8_t*>(recv_x);
+    a.recv_w = recv_w;
+    a.recv_src = recv_src;
+    a.status = status;
+    // Equal 16-byte-multiple chunks, each fitting one ring stage.
+    const uint32_t cap = ep::dispatch_stage_capacity(smem_optin);
+    if (cap < 16) return EP_ERR_UNSUPPORTED;
+    const uint32_t n_chunks = (a.row_bytes + cap - 1) / cap;
+    const uint32_t per = (a.row_bytes + n_chunks - 1) / n_chunks;
+    a.chunk_bytes = (per + 15u) & ~15u;
+    a.n_chunks = (a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes;
+    a.stage_bytes = a.chunk_bytes;
+    return from_cuda(ep::launch_dispatch(a, sms_in_effect(sm_count), smem_optin,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv, const int32_t* slot,
+                       const float* topk_w, int64_t T, int64_t H, int K, uint16_t* y,
+                       int32_t* status, void* stream) {
+    if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || num_recv < 0)
+        return EP_ERR_INVALID;
+    if (T * static_cast<int64_t>(K) >= (int64_t{1} << 31) || num_recv >= (int64_t{1} << 31) ||
+        H * 2 > 0x7FFFFFF0)
+        return EP_ERR_UNSUPPORTED;
+    if (T == 0) return EP_OK;
+    if (slot == nullptr || topk_w == nullptr || y == nullptr ||
+        (num_recv > 0 && expert_out == nullptr))
+        return EP_ERR_INVALID;
+    if (!aligned(expert_out, 16) || !aligned(y, 16) || !aligned(slot, 4) || !aligned(topk_w, 4) ||
+        !aligned(status, 4))
+        return EP_ERR_INVALID;
+    int sm_count = 0, smem_optin = 0;
+    if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
+    ep::CombineArgs a{};
+    a.expert_out = reinterpret_cast<const uint8_t*>(expert_out);
+    a.num_recv = num_recv;
+    a.slot = slot;
+    a.topk_w = topk_w;
+    a.T = T;
+    a.row_bytes = static_cast<uint32_t>(H * 2);
+    a.K = K;
+    a.y = reinterpret_cast<uint8_t*>(y);
+    a.status = status;
+    return from_cuda(
+        ep::launch_combine(a, sms_in_effect(sm_count), static_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_get_status(const int32_t* status, void* stream) {
+    if (status == nullptr) return EP_ERR_INVALID;
+    int32_t v = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&v, status, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return EP_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return EP_ERR_CUDA;
+    return static_cast<ep_status_t>(v);
+}
+
+const char* ep_status_string(ep_status_t s) {
+    switch (s) {
+        case EP_OK: return "ok";
+        case EP_ERR_INVALID: return "invalid argument";
+        case EP_ERR_UNSUPPORTED: return "size beyond the supported limits";
+        case EP_ERR_CUDA: return "CUDA runtime error";
+        case EP_ERR_TIMEOUT: return "bounded device wait gave up";
+        case EP_ERR_BAD_EXPERT: return "expert id outside [0, E) and not -1";
+        case EP_ERR_BAD_SLOT: return "slot beyond the receive buffer";
+        case EP_ERR_WORKSPACE: return "layout workspace too small";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,162 @@
+/*
+ * ep.h -- C ABI of the GB300 (sm_103a) MoE token dispatch / combine library
+ * (libep_gb300.so).
+ *
+ * Sources this interface follows (web pages; cited by title and section):
+ *  [DeepEP-TMA]  "How DeepEP Utilizes TMA Instructions for Minimal SM Usage on
+ *                Hopper GPUs" (instagit.com deep-dive on DeepSeek's DeepEP).
+ *  [TMA-note]    TMA study note, mkbk-pku.cn (in Chinese): sections "Hopper
+ *                architecture -- TMA" and "other TMA features".
+ *  [TMA-atlas]   "tensor-memory-accelerator" (semiaifoundry.com atlas).
+ *
+ * What the library computes. DeepEP's dispatch takes a token matrix, a top-k
+ * routing table and its weights ([DeepEP-TMA] "Practical Code Examples":
+ * buffer.dispatch(hidden_states, topk_idx, topk_weights, num_experts)) and
+ * copies every token row into a receive buffer of the expert it is routed to
+ * ([DeepEP-TMA] "Asynchronous Copy Primitives", the receive loop). On one GPU
+ * that is a pure HBM-to-HBM layout transform:
+ *
+ *   layout   counts[e]  = #{(t,k) : topk_idx[t,k] == e}
+ *            offsets    = exclusive prefix of counts, offsets[E] = R
+ *            slot[t,k]  = row of (t,k) in the receive buffer: experts in
+ *                         ascending order, each expert's rows contiguous and
+ *                         in ascending (t, k) order
+ *   dispatch recv_x[slot[t,k], :] = x[t, :]              (bitwise copy)
+ *   combine  y[t, :] = bf16_rne( sum over k = 0..K-1, in that order, as an
+ *                      fp32 fused-multiply-add chain starting from +0.0f, of
+ *                      topk_w[t,k] * float(expert_out[slot[t,k], :]) )
+ *
+ * The pages describe neither the layout call nor combine; the stable order,
+ * the masking rule and the combine arithmetic above are this library's
+ * readings (plainest reading of the MoE problem the pages state), chosen so
+ * that every result has exactly one correct value.
+ *
+ * Conventions (all entry points):
+ *  - Types. bf16 tensors are passed as uint16_t bit patterns (IEEE binary32
+ *    upper half). Matrices are row-major and dense (row stride = width).
+ *  - Memory. Every pointer except where noted is a DEVICE pointer on the
+ *    current CUDA device. The caller allocates and owns every buffer,
+ *    including the receive buffer and the layout workspace; the library
+ *    allocates nothing and keeps no state besides the SM budget. (On one GPU
+ *    this is what remains of DeepEP's pre-allocated communication Buffer.)
+ *  - Streams. `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream). Every call only enqueues work and returns; ordering on
+ *    the stream replaces the `event` DeepEP's dispatch returns.
+ *  - Errors. Argument problems found on the host return at once, before any
+ *    work is enqueued. Problems found on the device (an expert id out of
+ *    range, a slot beyond the receive buffer, a bounded wait that gave up)
+ *    skip the offending row and write their code into the optional device
+ *    status word (first error wins); ep_get_status() reads it.
+ *  - Alignment. x, recv_x, expert_out and y must be 16-byte aligned and H a
+ *    multiple of 8 (rows are moved with 16-byte bulk copies, which need
+ *    16-byte aligned addresses and sizes: [TMA-note] "Hopper architecture --
+ *    TMA"). topk_idx must be 8-byte aligned; the int32/fp32 arrays 4-byte.
+ *  - Masking. topk_idx[t,k] == -1 marks an unused entry: it gets slot -1 and
+ *    every call skips it. Any other id outside [0, E) is skipped too and
+ *    reported as EP_ERR_BAD_EXPERT.
+ *  - Limits. 1 <= K <= 32, 1 <= E <= EP_MAX_EXPERTS, T*K < 2^31.
+ *  - Threads. The SM budget is process-wide; concurrent calls from several
+ *    host threads are the caller's to order.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the shared library (built with hidden visibility by default). */
+#if defined(__GNUC__)
+#define EP_API __attribute__((visibility("default")))
+#else
+#define EP_API
+#endif
+
+#define EP_MAX_TOPK 32
+#define EP_MAX_EXPERTS 4096
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID = 1,      /* bad argument (host): null, negative size, misalignment, K, H%8 */
+    EP_ERR_UNSUPPORTED = 2,  /* sizes beyond the documented limits (host) */
+    EP_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed (host) */
+    EP_ERR_TIMEOUT = 4,      /* device: a bounded mbarrier wait gave up (~2 s) */
+    EP_ERR_BAD_EXPERT = 5,   /* device: topk_idx outside [0, E) and not -1 */
+    EP_ERR_BAD_SLOT = 6,     /* device: slot >= num_recv (receive buffer too small) */
+    EP_ERR_WORKSPACE = 7     /* host: layout workspace smaller than required */
+} ep_status_t;
+
+/* SM budget, after DeepEP's Buffer.set_num_sms ([DeepEP-TMA] "Minimal SM
+ * Occupancy Configuration"): dispatch and combine launch one CTA per SM on at
+ * most this many SMs. 0 means all SMs. Values above the device's SM count
+ * are clamped at launch. Returns the stored budget, or -1 (and changes
+ * nothing) if num_sms < 0. */
+EP_API int ep_set_num_sms(int num_sms);
+
+/* The stored SM budget (0 = all). */
+EP_API int ep_get_num_sms(void);
+
+/* The number of SMs dispatch/combine will use on the current device: the
+ * budget clamped to [1, SM count]. Returns -1 if the device can't be queried. */
+EP_API int ep_num_sms_in_effect(void);
+
+/* Bytes of device workspace ep_get_dispatch_layout needs for these sizes
+ * (0 when none; then `workspace` may be NULL). Depends on sizes only. */
+EP_API size_t ep_layout_workspace_bytes(int64_t T, int K, int E);
+
+/* Layout (per-expert histogram, exclusive prefix sums and per-(token,k)
+ * destination slot).
+ *   topk_idx   int64 [T][K]   routing table (DeepEP's topk_idx)
+ *   counts     int32 [E]      out: rows per expert
+ *   offsets    int32 [E+1]    out: first row of each expert; offsets[E] = R
+ *   slot       int32 [T][K]   out: receive row of (t,k), -1 if skipped
+ *   workspace  device scratch of ep_layout_workspace_bytes(T,K,E) bytes
+ *   status     int32 device word, nullable (device errors: BAD_EXPERT)
+ * T == 0 is valid (counts and offsets are zeroed). */
+EP_API ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, int E,
+                                   int32_t* counts, int32_t* offsets, int32_t* slot,
+                                   void* workspace, size_t workspace_bytes,
+                                   int32_t* status, void* stream);
+
+/* Dispatch ([DeepEP-TMA] "Asynchronous Copy Primitives"): each warp's elected
+ * lane bulk-copies token-row chunks global -> shared (completion on an
+ * mbarrier) and shared -> global, once into shared memory and K times out.
+ *   x          bf16 [T][H]
+ *   slot       int32 [T][K]  from ep_get_dispatch_layout
+ *   topk_w     fp32 [T][K]   nullable; needed only for recv_w
+ *   num_recv   rows of recv_x (>= R = offsets[E]); larger slots -> BAD_SLOT
+ *   recv_x     bf16 [num_recv][H] out
+ *   recv_w     fp32 [num_recv] out, nullable: recv_w[slot[t,k]] = topk_w[t,k]
+ *   recv_src   int32 [num_recv] out, nullable: recv_src[slot[t,k]] = t*K + k
+ * Rows of recv_x no (t,k) maps to are left untouched. */
+EP_API ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K,
+                        const int32_t* slot, const float* topk_w, int64_t num_recv,
+                        uint16_t* recv_x, float* recv_w, int32_t* recv_src,
+                        int32_t* status, void* stream);
+
+/* Combine: weighted gather of the K expert rows of every token back into
+ * token order (arithmetic in the header comment above).
+ *   expert_out bf16 [num_recv][H]  rows in receive order
+ *   slot       int32 [T][K]
+ *   topk_w     fp32 [T][K]         routing weights in token order
+ *   y          bf16 [T][H] out
+ * A token whose K entries are all skipped gets +0.0. */
+EP_API ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv,
+                       const int32_t* slot, const float* topk_w,
+                       int64_t T, int64_t H, int K,
+                       uint16_t* y, int32_t* status, void* stream);
+
+/* Synchronises `stream`, then returns the device status word (an
+ * ep_status_t), or EP_ERR_CUDA if the copy fails. Does not reset it. */
+EP_API ep_status_t ep_get_status(const int32_t* status, void* stream);
+
+/* Static description of a status code. */
+EP_API const char* ep_status_string(ep_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EP_GB300_H */

@@ -1,0 +1,104 @@
+"""The C-ABI library loads and exports every symbol include/ep.h declares,
+and its host-side argument checks answer without touching a GPU (CPU only:
+every call below returns before any CUDA runtime call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ep():
+    from combine_movement_gb300 import build
+    build.build()
+    from combine_movement_gb300 import ep as mod
+    return mod
+
+
+def declared_symbols():
+    hdr = open(os.path.join(ROOT, "include", "ep.h")).read()
+    return sorted(set(re.findall(r"EP_API\s+[\w\s\*]+?\b(ep_\w+)\s*\(", hdr)))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_symbols()
+    for want in ("ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_set_num_sms"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(ep):
+    names = declared_symbols()
+    assert len(names) >= 9
+    lib = ctypes.CDLL(ep.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", ep.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if l.strip()}
+    assert set(names) <= exported
+    # hidden visibility: nothing but the ABI (and no C++ internals) leaks out
+    assert not [s for s in exported if s.startswith("_ZN2ep")]
+
+
+def test_sm_budget_is_stored(ep):
+    old = ep.ep_get_num_sms()
+    try:
+        assert ep.ep_set_num_sms(24) == 24
+        assert ep.ep_get_num_sms() == 24
+        assert ep.ep_set_num_sms(-3) == -1
+        assert ep.ep_get_num_sms() == 24
+        assert ep.ep_set_num_sms(0) == 0
+    finally:
+        ep.ep_set_num_sms(old)
+
+
+def test_status_strings(ep):
+    for code in range(8):
+        s = ep.ep_status_string(code)
+        assert s and s != "unknown status"
+    assert ep.ep_status_string(99) == "unknown status"
+
+
+def test_workspace_bytes(ep):
+    assert ep.ep_layout_workspace_bytes(128, 8, 256) == 0          # one fused launch
+    big = ep.ep_layout_workspace_bytes(4096, 8, 256)
+    assert big > 0 and big % 4 == 0
+    assert big == 4 * 256 * ((4096 * 8 + 4095) // 4096)            # E x tiles int32
+    assert ep.ep_layout_workspace_bytes(4096, 33, 256) == 0        # invalid -> 0
+    assert ep.ep_layout_workspace_bytes(10, 2, 5000) == 0
+
+
+def _raw(ep):
+    return ep.lib
+
+
+def test_host_argument_checks(ep):
+    lib = _raw(ep)
+    A = 0x10000  # a fake, 16-byte aligned "device" address; never dereferenced
+    # dispatch: H not a multiple of 8, K out of range, misaligned x, null slot
+    assert lib.ep_dispatch(A, 4, 12, 2, A, None, 8, A, None, None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch(A, 4, 16, 33, A, None, 8, A, None, None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch(A, 4, 16, 0, A, None, 8, A, None, None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch(A + 8, 4, 16, 2, A, None, 8, A, None, None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch(A, 4, 16, 2, None, None, 8, A, None, None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch(A, 4, 16, 2, A, None, 8, A, A, None, None, None) == ep.EP_ERR_INVALID  # recv_w needs topk_w
+    assert lib.ep_dispatch(A, -1, 16, 2, A, None, 8, A, None, None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch(A, 1 << 30, 16, 8, A, None, 8, A, None, None, None, None) == ep.EP_ERR_UNSUPPORTED
+    assert lib.ep_dispatch(None, 0, 16, 2, None, None, 0, None, None, None, None, None) == ep.EP_OK  # T == 0
+    # combine
+    assert lib.ep_combine(A, 8, A, A, 4, 16, 2, None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_combine(A, 8, A, None, 4, 16, 2, A, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_combine(A + 4, 8, A, A, 4, 16, 2, A, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_combine(A, 8, A, A, 4, 10, 2, A, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_combine(None, 0, None, None, 0, 16, 2, None, None, None) == ep.EP_OK
+    # layout
+    assert lib.ep_get_dispatch_layout(A, 4, 2, 0, A, A, A, None, 0, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_get_dispatch_layout(A, 4, 2, 5000, A, A, A, None, 0, None, None) == ep.EP_ERR_UNSUPPORTED
+    assert lib.ep_get_dispatch_layout(A + 4, 4, 2, 8, A, A, A, None, 0, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_get_dispatch_layout(A, 4096, 8, 256, A, A, A, None, 0, None, None) == ep.EP_ERR_WORKSPACE
+    assert lib.ep_get_dispatch_layout(A, 4096, 8, 256, A, A, A, A, 64, None, None) == ep.EP_ERR_WORKSPACE
+    assert lib.ep_get_status(None, None) == ep.EP_ERR_INVALID

@@ -1,0 +1,283 @@
+"""GPU path (through the C ABI) against the CPU oracle, element by element.
+
+Layout and dispatch must match bit for bit; combine within 1 bf16 ulp (the
+tolerance of the fixed-order fp32 reduction; the fma chain is the same on
+both sides, so the tests also require bit-exact equality where noted).
+Every workload of the benchmark is checked at full size, at the SM budgets
+the benchmark uses, plus edge cases (empty, ragged, masked, invalid ids,
+maximum K and E, multi-chunk rows).
+"""
+from __future__ import annotations
+
+import dataclasses
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_movement_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+CANARY = 0x7FA5  # a NaN bit pattern no copied row carries
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    from combine_movement_gb300 import build
+    build.build()
+    yield
+    from combine_movement_gb300 import ep
+    ep.ep_set_num_sms(0)
+
+
+@pytest.fixture(scope="module")
+def ep():
+    from combine_movement_gb300 import ep as mod
+    return mod
+
+
+@functools.lru_cache(maxsize=None)
+def _oracle():
+    return oracle.Oracle()
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def from_bits(b: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+
+
+def ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    def ordered(u):
+        u = u.astype(np.int32)
+        return np.where(u & 0x8000, -(u & 0x7FFF), u)
+    return np.abs(ordered(a) - ordered(b))
+
+
+@dataclasses.dataclass
+class Ref:
+    counts: np.ndarray
+    offsets: np.ndarray
+    slot: np.ndarray
+    status: int
+    recv_x: np.ndarray
+    recv_w: np.ndarray
+    recv_src: np.ndarray
+    expert_out: np.ndarray
+    y: np.ndarray
+
+
+def oracle_path(inp: W.Inputs, num_recv: int, expert_scale: float) -> Ref:
+    o = _oracle()
+    idx = inp.topk_idx.numpy()
+    counts, offsets, slot, st = o.layout(idx, inp.wl.E)
+    recv_x, recv_w, recv_src = o.dispatch(inp.x_bits(), slot, num_recv, inp.topk_w.numpy(),
+                                          fill=CANARY)
+    eo = bits(W.expert_standin(from_bits(recv_x), expert_scale))
+    y = o.combine(eo, slot, inp.topk_w.numpy())
+    return Ref(counts, offsets, slot, st, recv_x, recv_w, recv_src, eo, y)
+
+
+def gpu_path(ep, inp: W.Inputs, num_recv: int, expert_out: np.ndarray, num_sms: int = 0,
+             stream=None):
+    dev = torch.device("cuda:0")
+    E = inp.wl.E
+    ep.ep_set_num_sms(num_sms)
+    idx = inp.topk_idx.to(dev)
+    w = inp.topk_w.to(dev)
+    x = inp.x.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    T, K = idx.shape
+    counts = torch.full((E,), -7, dtype=torch.int32, device=dev)
+    offsets = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
+    slot = torch.full((T, K), -7, dtype=torch.int32, device=dev)
+    nws = ep.ep_layout_workspace_bytes(T, K, E)
+    ws = torch.full((max(nws, 4),), 0x55, dtype=torch.uint8, device=dev) if nws else None
+    recv_x = torch.full((num_recv, inp.wl.H), CANARY, dtype=torch.int16,
+                        device=dev).view(torch.bfloat16)
+    recv_w = torch.full((num_recv,), float("nan"), dtype=torch.float32, device=dev)
+    recv_src = torch.full((num_recv,), -1, dtype=torch.int32, device=dev)
+    y = torch.full((T, inp.wl.H), 3.0, dtype=torch.bfloat16, device=dev)
+    eo = from_bits(expert_out).to(dev)
+    ep.ep_get_dispatch_layout(idx, E, counts, offsets, slot, ws, status, stream)
+    ep.ep_dispatch(x, slot, recv_x, w, recv_w, recv_src, status, stream)
+    ep.ep_combine(eo, slot, w, y, status, stream)
+    st = ep.ep_get_status(status, stream)
+    torch.cuda.synchronize()
+    return dict(counts=counts.cpu().numpy(), offsets=offsets.cpu().numpy(),
+                slot=slot.cpu().numpy(), recv_x=bits(recv_x), recv_w=recv_w.cpu().numpy(),
+                recv_src=recv_src.cpu().numpy(), y=bits(y), status=st)
+
+
+def assert_parity(got: dict, ref: Ref, exact_combine: bool = True) -> None:
+    assert got["status"] == ref.status, (got["status"], ref.status)
+    assert np.array_equal(got["counts"], ref.counts), "counts"
+    assert np.array_equal(got["offsets"], ref.offsets), "offsets"
+    assert np.array_equal(got["slot"], ref.slot), "slot"
+    assert np.array_equal(got["recv_x"], ref.recv_x), "recv_x (incl. untouched canary rows)"
+    assert np.array_equal(got["recv_w"], ref.recv_w, equal_nan=True), "recv_w"
+    assert np.array_equal(got["recv_src"], ref.recv_src), "recv_src"
+    d = ulp_distance(got["y"], ref.y)
+    assert int(d.max(initial=0)) <= 1, f"combine off by {int(d.max())} ulp"
+    if exact_combine:
+        assert np.array_equal(got["y"], ref.y), f"combine: {int((d > 0).sum())} elements differ by 1 ulp"
+
+
+@functools.lru_cache(maxsize=2)
+def _case(name: str):
+    wl = {"tiny": W.TINY, "decode": W.DECODE, "skewed": W.SKEWED,
+          "deepseek": W.DEEPSEEK_PREFILL}.get(name)
+    if wl is None:
+        T, H = (int(v) for v in name.split(":"))
+        wl = W.sweep(T, H)
+    inp = W.make_inputs(wl)
+    R = wl.T * wl.K
+    return inp, oracle_path(inp, R, wl.expert_scale)
+
+
+@pytest.mark.parametrize("name,budgets", [
+    ("tiny", (0, 1, 8)),
+    ("decode", (0, 16, 24)),
+    ("skewed", (0, 24)),
+    ("deepseek", (0, 8, 16, 24, 48)),
+])
+def test_workloads_full_size(ep, name, budgets):
+    inp, ref = _case(name)
+    for b in budgets:
+        got = gpu_path(ep, inp, inp.wl.T * inp.wl.K, ref.expert_out, num_sms=b)
+        assert_parity(got, ref)
+
+
+@pytest.mark.parametrize("T", W.SWEEP_T)
+@pytest.mark.parametrize("H", W.SWEEP_H)
+def test_size_sweep(ep, T, H):
+    inp, ref = _case(f"{T}:{H}")
+    budgets = (0, 8, 16, 24, 48) if T * H <= 4096 * 7168 else (0, 24)
+    for b in budgets:
+        got = gpu_path(ep, inp, T * 8, ref.expert_out, num_sms=b)
+        assert_parity(got, ref)
+
+
+def _custom(T, H, E, K, seed=7, mask=0.0, routing="uniform"):
+    wl = W.Workload(f"edge-T{T}-H{H}-E{E}-K{K}", T=T, H=H, E=E, K=K, seed=seed,
+                    mask_frac=mask, routing=routing)
+    return W.make_inputs(wl)
+
+
+@pytest.mark.parametrize("T,H,E,K,mask", [
+    (1, 8, 1, 1, 0.0),          # smallest everything; 16-byte rows
+    (3, 24, 2, 2, 0.0),         # ragged 48-byte rows (partial column block)
+    (33, 520, 5, 3, 0.0),       # odd sizes, T*K not a multiple of 32
+    (257, 16384, 16, 4, 0.0),   # multi-chunk rows (32 KB)
+    (300, 7176, 64, 8, 0.0),    # H not a multiple of the chunk or 512-byte block
+    (500, 1024, 128, 6, 0.3),   # masked entries (-1)
+    (64, 256, 4096, 8, 0.0),    # maximum expert count, mostly empty experts
+    (2048, 256, 4096, 8, 0.0),  # maximum expert count, multi-tile layout
+    (40, 64, 40, 32, 0.0),      # maximum K (generic combine path)
+    (100, 128, 16, 12, 0.1),    # K above the specialised range, masked
+    (9000, 64, 256, 1, 0.0),    # K = 1, multi-tile layout
+])
+def test_edge_shapes(ep, T, H, E, K, mask):
+    inp = _custom(T, H, E, K, mask=mask)
+    R_valid = int((inp.topk_idx >= 0).sum())
+    num_recv = R_valid + 3  # spare rows must stay untouched
+    ref = oracle_path(inp, num_recv, 1.0)
+    assert int(ref.offsets[-1]) == R_valid
+    for b in (0, 3):
+        assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=b), ref)
+
+
+def test_empty_batch(ep):
+    inp = _custom(0, 64, 8, 2)
+    ref = oracle_path(inp, 0, 1.0)
+    got = gpu_path(ep, inp, 0, ref.expert_out)
+    assert got["status"] == 0
+    assert np.array_equal(got["counts"], np.zeros(8, np.int32))
+    assert np.array_equal(got["offsets"], np.zeros(9, np.int32))
+
+
+def test_hot_expert_and_duplicates(ep):
+    # every token sends all K picks to expert 0 or repeats an expert
+    T, H, E, K = 1500, 512, 8, 4
+    inp = _custom(T, H, E, K)
+    idx = inp.topk_idx.clone()
+    idx[: T // 2] = 0
+    idx[T // 2:, 1] = idx[T // 2:, 0]
+    inp = dataclasses.replace(inp, topk_idx=idx.contiguous())
+    ref = oracle_path(inp, T * K, 1.0)
+    assert int(ref.counts[0]) >= 2 * T  # the hot expert
+    for b in (0, 5):
+        assert_parity(gpu_path(ep, inp, T * K, ref.expert_out, num_sms=b), ref)
+
+
+def test_bad_expert_ids_are_skipped_and_reported(ep):
+    inp = _custom(700, 64, 32, 4)
+    idx = inp.topk_idx.clone()
+    idx[5, 1] = 32
+    idx[600, 3] = -9
+    idx[17, 0] = -1
+    inp = dataclasses.replace(inp, topk_idx=idx.contiguous())
+    ref = oracle_path(inp, 700 * 4, 1.0)
+    assert ref.status == oracle.BAD_EXPERT
+    got = gpu_path(ep, inp, 700 * 4, ref.expert_out)
+    assert got["status"] == ep.EP_ERR_BAD_EXPERT
+    got["status"] = ref.status
+    assert_parity(got, ref)
+
+
+def test_receive_buffer_too_small_is_reported(ep):
+    inp = _custom(64, 64, 4, 2)
+    ref = oracle_path(inp, 64 * 2, 1.0)
+    dev = torch.device("cuda:0")
+    slot = torch.from_numpy(ref.slot).to(dev)
+    x = inp.x.to(dev)
+    small = torch.zeros((100, 64), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ep.ep_set_num_sms(0)
+    ep.ep_dispatch(x, slot, small, status=status)
+    assert ep.ep_get_status(status) == ep.EP_ERR_BAD_SLOT
+    # rows that fit were written
+    ok = ref.slot.reshape(-1) < 100
+    rows = ref.slot.reshape(-1)[ok]
+    assert np.array_equal(bits(small)[rows], ref.recv_x[rows])
+    status.zero_()
+    y = torch.empty((64, 64), dtype=torch.bfloat16, device=dev)
+    ep.ep_combine(small, slot, inp.topk_w.to(dev), y, status=status)
+    assert ep.ep_get_status(status) == ep.EP_ERR_BAD_SLOT
+
+
+def test_combine_closed_forms_on_gpu(ep):
+    # all weights 1 with identity experts gives bf16(K*x); one-hot gives x
+    T, H, E, K = 512, 7168, 256, 8
+    inp = _custom(T, H, E, K)
+    dev = torch.device("cuda:0")
+    ep.ep_set_num_sms(0)
+    counts, offsets, slot = ep.get_dispatch_layout(inp.topk_idx.to(dev), E)
+    x = inp.x.to(dev)
+    recv = ep.dispatch(x, slot, T * K)
+    ones = torch.ones((T, K), dtype=torch.float32, device=dev)
+    y = ep.combine(recv, slot, ones)
+    want = (inp.x.float() * K).to(torch.bfloat16)
+    assert np.array_equal(bits(y), bits(want))
+    oh = torch.zeros((T, K), dtype=torch.float32, device=dev)
+    oh[:, K - 1] = 1.0
+    assert np.array_equal(bits(ep.combine(recv, slot, oh)), bits(inp.x))
+
+
+def test_side_stream_and_repeat_determinism(ep):
+    inp, ref = _case("skewed")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = gpu_path(ep, inp, inp.wl.T * inp.wl.K, ref.expert_out, num_sms=24, stream=s)
+    b = gpu_path(ep, inp, inp.wl.T * inp.wl.K, ref.expert_out, num_sms=24)
+    assert_parity(a, ref)
+    for k in a:
+        assert np.array_equal(a[k], b[k], equal_nan=True)
