@@ -31,7 +31,7 @@ namespace ep {
 namespace {
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
-constexpr size_t kRunSmemBudget = 48 * 1024;  // per-warp expert counters of the rank kernel
+constexpr size_t kRunSmemBudget = 64 * 1024;  // per-warp expert counters of the rank kernel
 constexpr int kTileRounds = 4;                // rounds per warp per tile (multi-tile path)
 constexpr int kFusedRounds = 8;               // rounds per warp for the single-block path
 constexpr int kScanThreads = 1024;
@@ -244,6 +244,13 @@ cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,
                           int32_t* offsets, int32_t* slot, int32_t* tile_counts,
                           const LayoutPlan& p, int32_t* status, cudaStream_t stream) {
     const int threads = p.warps * 32;
+    // The ranking kernel's dynamic shared memory can exceed the default 48 KB
+    // (it also holds a few static words for the block scan).
+    cudaError_t err = cudaFuncSetAttribute(p.num_tiles == 1 ? layout_rank_kernel<true>
+                                                            : layout_rank_kernel<false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kRunSmemBudget));
+    if (err != cudaSuccess) return err;
     if (p.num_tiles == 1) {
         layout_rank_kernel<true><<<1, threads, p.smem, stream>>>(
             idx, N, E, p.rounds, p.tile, 1, nullptr, counts, offsets, slot, status);
