@@ -59,6 +59,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_dispatch.restype = i32
     lib.ep_combine.argtypes = [p, i64, p, p, i64, i64, i32, p, p, p]
     lib.ep_combine.restype = i32
+    lib.ep_get_dispatch_layout_noalloc.argtypes = [p, i64, i32, i32, p, p, p, p, p]
+    lib.ep_get_dispatch_layout_noalloc.restype = i32
     lib.ep_get_status.argtypes = [p, p]
     lib.ep_get_status.restype = i32
     lib.ep_status_string.argtypes = [i32]
@@ -132,6 +134,23 @@ def ep_get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, counts: tor
         _ptr(slot, torch.int32, "slot"), _ptr(workspace, None, "workspace"), ws_bytes,
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(code, "ep_get_dispatch_layout")
+
+
+def ep_get_dispatch_layout_noalloc(topk_idx: torch.Tensor, num_experts: int,
+                                   counts: torch.Tensor, offsets: torch.Tensor,
+                                   slot: torch.Tensor, status: Optional[torch.Tensor] = None,
+                                   stream=None) -> None:
+    """Layout for callers that cannot allocate: the scratch is the library's
+    static device array (EP_NOALLOC_SCRATCH_BYTES), shared by every call."""
+    T, K = topk_idx.shape
+    code = lib.ep_get_dispatch_layout_noalloc(
+        _ptr(topk_idx, torch.int64, "topk_idx"), T, K, int(num_experts),
+        _ptr(counts, torch.int32, "counts"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(slot, torch.int32, "slot"), _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(code, "ep_get_dispatch_layout_noalloc")
+
+
+EP_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 def ep_dispatch(x: torch.Tensor, slot: torch.Tensor, recv_x: torch.Tensor,

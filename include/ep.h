@@ -149,6 +149,28 @@ EP_API ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv,
                        int64_t T, int64_t H, int K,
                        uint16_t* y, int32_t* status, void* stream);
 
+/* Layout without a workspace argument, for callers that cannot allocate
+ * device memory. The pages have no counterpart; this is a library addition.
+ * Such callers include a serving engine that reserved nearly all of HBM up
+ * front for weights and KV cache (an extra cudaMalloc would fail or fragment
+ * its pool) and latency-critical pipelines (cudaMalloc/cudaFree may
+ * synchronise the whole device). Same arguments and results as
+ * ep_get_dispatch_layout, but the layout's scratch lives in a static device
+ * array of EP_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps
+ * until the process exits; this call allocates nothing.
+ *  - Limit: sizes whose ep_layout_workspace_bytes(T,K,E) exceeds
+ *    EP_NOALLOC_SCRATCH_BYTES are rejected with EP_ERR_UNSUPPORTED.
+ *  - Set-up: the first call on each device (with that device current) looks
+ *    up the array's device address; make that first call before any stream
+ *    capture.
+ *  - Sharing: all calls share the array. Calls that overlap on the GPU (other
+ *    streams or host threads) race on it; order them. Nothing in it needs to
+ *    start at zero: each call rewrites what it reads. */
+#define EP_NOALLOC_SCRATCH_BYTES (1u << 20)
+EP_API ep_status_t ep_get_dispatch_layout_noalloc(const int64_t* topk_idx, int64_t T, int K, int E,
+                                                  int32_t* counts, int32_t* offsets, int32_t* slot,
+                                                  int32_t* status, void* stream);
+
 /* Synchronises `stream`, then returns the device status word (an
  * ep_status_t), or EP_ERR_CUDA if the copy fails. Does not reset it. */
 EP_API ep_status_t ep_get_status(const int32_t* status, void* stream);
