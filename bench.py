@@ -98,7 +98,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -145,41 +145,57 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the step
 
+class Buffers:
+    """Device buffers of one step (inputs, layout, receive buffer, output)."""
+
+    def __init__(self, ep, wl: W.Workload, dev: torch.device):
+        T, H, E, K = wl.T, wl.H, wl.E, wl.K
+        self.x = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.idx = torch.empty((T, K), dtype=torch.int64, device=dev)
+        self.w = torch.empty((T, K), dtype=torch.float32, device=dev)
+        self.counts = torch.empty(E, dtype=torch.int32, device=dev)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        self.slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+        nws = ep.ep_layout_workspace_bytes(T, K, E)
+        self.ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+        self.recv_x = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+
 class Step:
-    """Device buffers of one workload and the three calls of one step."""
+    """The three calls of one step on a set of device buffers."""
 
     def __init__(self, ep, inp: W.Inputs, dev: torch.device):
         wl = inp.wl
         self.ep, self.wl, self.dev = ep, wl, dev
         self.T, self.H, self.E, self.K = wl.T, wl.H, wl.E, wl.K
         self.R = wl.T * wl.K
-        self.idx = inp.topk_idx.to(dev)
-        self.w = inp.topk_w.to(dev)
-        self.x = inp.x.to(dev)
-        self.counts = torch.empty(self.E, dtype=torch.int32, device=dev)
-        self.offsets = torch.empty(self.E + 1, dtype=torch.int32, device=dev)
-        self.slot = torch.empty((self.T, self.K), dtype=torch.int32, device=dev)
-        nws = ep.ep_layout_workspace_bytes(self.T, self.K, self.E)
-        self.ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
-        self.layout_launches = 3 if nws else 1
-        self.recv_x = torch.empty((self.R, self.H), dtype=torch.bfloat16, device=dev)
-        self.y = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=dev)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.b = Buffers(ep, wl, dev)
+        self.b.x.copy_(inp.x)
+        self.b.idx.copy_(inp.topk_idx)
+        self.b.w.copy_(inp.topk_w)
+        self.layout_launches = ep.layout_launches(self.T, self.K, self.E)
         # the experts between dispatch and combine are a fixed stand-in
-        self.layout()
-        self.dispatch()
-        self.expert_out = W.expert_standin(self.recv_x, wl.expert_scale)
+        self.layout(self.b)
+        self.dispatch(self.b)
+        self.expert_out = W.expert_standin(self.b.recv_x, wl.expert_scale)
         torch.cuda.synchronize(dev)
 
-    def layout(self, stream=None):
-        self.ep.ep_get_dispatch_layout(self.idx, self.E, self.counts, self.offsets, self.slot,
-                                       self.ws, self.status, stream)
+    def layout(self, b: Buffers, stream=None):
+        self.ep.ep_get_dispatch_layout(b.idx, self.E, b.counts, b.offsets, b.slot, b.ws,
+                                       b.status, stream)
 
-    def dispatch(self, stream=None):
-        self.ep.ep_dispatch(self.x, self.slot, self.recv_x, None, None, None, self.status, stream)
+    def dispatch(self, b: Buffers, stream=None):
+        self.ep.ep_dispatch(b.x, b.slot, b.recv_x, None, None, None, b.status, stream)
 
-    def combine(self, stream=None):
-        self.ep.ep_combine(self.expert_out, self.slot, self.w, self.y, self.status, stream)
+    def combine(self, b: Buffers, stream=None):
+        self.ep.ep_combine(self.expert_out, b.slot, b.w, b.y, b.status, stream)
+
+    def run(self, b: Buffers, stream=None):
+        self.layout(b, stream)
+        self.dispatch(b, stream)
+        self.combine(b, stream)
 
     @property
     def launches_per_step(self) -> int:
@@ -207,9 +223,7 @@ def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch
     with per-kernel CUDA events recorded on the launching stream."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            step.layout(stream)
-            step.dispatch(stream)
-            step.combine(stream)
+            step.run(step.b, stream)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
@@ -222,11 +236,11 @@ def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch
         for i in range(steps):
             e = ev[i]
             e[0].record(stream)
-            step.layout(stream)
+            step.layout(step.b, stream)
             e[1].record(stream)
-            step.dispatch(stream)
+            step.dispatch(step.b, stream)
             e[2].record(stream)
-            step.combine(stream)
+            step.combine(step.b, stream)
             e[3].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
@@ -241,38 +255,59 @@ def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch
             "clocks": sampler.summary() if sampler else None}
 
 
-def time_e2e(step: Step, inp: W.Inputs, steps: int, warmup: int, stream) -> dict:
-    """Same step through the public API with host-resident inputs: every step
-    copies x, topk_idx and topk_w from pinned host memory to the device and
-    reads y back, inside the timed region."""
+def time_e2e(step: Step, inp: W.Inputs, steps: int, warmup: int) -> dict:
+    """The same step through the public API with host-resident inputs: every
+    step copies x, topk_idx and topk_w from pinned host memory to the device
+    and reads y back, inside the timed region. Two device buffer sets and
+    separate copy streams let step i's copies overlap step i-1's kernels,
+    as a caller pipelining batches would."""
+    dev = step.dev
     hx = inp.x.pin_memory()
     hidx = inp.topk_idx.pin_memory()
     hw = inp.topk_w.pin_memory()
-    hy = torch.empty_like(step.y, device="cpu").pin_memory()
+    hy = [torch.empty(step.b.y.shape, dtype=step.b.y.dtype).pin_memory() for _ in range(2)]
+    bufs = [step.b, Buffers(step.ep, step.wl, dev)]
     h2d = hx.numel() * hx.element_size() + hidx.numel() * 8 + hw.numel() * 4
-    d2h = hy.numel() * hy.element_size()
+    d2h = hy[0].numel() * hy[0].element_size()
+    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    done = [torch.cuda.Event() for _ in range(2)]   # kernels of the buffer set finished
+    out = [torch.cuda.Event() for _ in range(2)]    # its y was read back
+    for e in done + out:
+        e.record(s_run)
 
-    def one():
-        step.x.copy_(hx, non_blocking=True)
-        step.idx.copy_(hidx, non_blocking=True)
-        step.w.copy_(hw, non_blocking=True)
-        step.layout(stream)
-        step.dispatch(stream)
-        step.combine(stream)
-        hy.copy_(step.y, non_blocking=True)
+    def one(i: int):
+        j = i % 2
+        b = bufs[j]
+        ready = torch.cuda.Event()
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(done[j])
+            b.x.copy_(hx, non_blocking=True)
+            b.idx.copy_(hidx, non_blocking=True)
+            b.w.copy_(hw, non_blocking=True)
+            ready.record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(ready)
+            s_run.wait_event(out[j])
+            step.run(b, s_run)
+            done[j].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[j])
+            hy[j].copy_(b.y, non_blocking=True)
+            out[j].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            one()
-        torch.cuda.synchronize()
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        for _ in range(steps):
-            one()
-        e.record(stream)
-        torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    for i in range(steps):
+        one(warmup + i)
+    s_in.wait_stream(s_out)
+    s_in.wait_stream(s_run)
+    end.record(s_in)
+    torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(end) / steps
     return {"ms_per_step": ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
@@ -339,7 +374,7 @@ def wl_desc(wl: W.Workload) -> str:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="deepseek-v3-prefill", choices=sorted(W.BY_NAME))
@@ -379,8 +414,8 @@ def main():
     ep.ep_set_num_sms(args.budget_sms)
     budget_run = time_steps(step, args.steps, args.warmup, dist_on, stream)
     ep.ep_set_num_sms(0)
-    e2e = time_e2e(step, inp, max(3, args.steps // 2), 3, stream)
-    st = ep.ep_get_status(step.status)
+    e2e = time_e2e(step, inp, max(3, min(args.steps, 200)), 3)
+    st = ep.ep_get_status(step.b.status)
     if st != 0:
         raise SystemExit(f"device status {st}: {ep.ep_status_string(st)}")
 

@@ -8,8 +8,9 @@
 // at +0.0f, one fused multiply-add per k in ascending k (entries with slot < 0
 // skipped), one bf16 round-to-nearest-even per output element.
 //
-// Mapping: persistent grid of one CTA per SM (the SM budget). A unit is one
-// 512-byte column block of one token row (32 lanes x 16 bytes); every warp
+// Mapping: persistent grid of one CTA per SM (the SM budget). A unit is
+// EP_COMBINE_UNROLL 512-byte column blocks of one token row (a block is 32
+// lanes x 16 bytes); every warp
 // takes a contiguous, equal range of units, so the load is balanced to within
 // one unit whatever T and the budget. For each token the warp reads slot and
 // weight once (lanes k < K) and broadcasts them with warp shuffles; each lane
@@ -26,9 +27,18 @@
 namespace ep {
 namespace {
 
+// Build-time shape (defaults are the tuned values).
+#ifndef EP_COMBINE_THREADS
+#define EP_COMBINE_THREADS 512
+#endif
+#ifndef EP_COMBINE_UNROLL
+#define EP_COMBINE_UNROLL 2
+#endif
+
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
-constexpr int kCombineThreads = 512;
-constexpr uint32_t kColBytes = 512;  // row bytes one warp covers per unit
+constexpr int kCombineThreads = EP_COMBINE_THREADS;
+constexpr int kUnroll = EP_COMBINE_UNROLL;
+constexpr uint32_t kColBytes = 512;  // row bytes one warp covers per column block
 
 __device__ __forceinline__ uint4 ld_expert(const uint8_t* p) {
     uint4 v;
@@ -59,12 +69,15 @@ __device__ __forceinline__ uint4 round8(const float (&acc)[8]) {
 }
 
 // KT > 0: K == KT known at compile time (slots, row pointers and weights in
-// registers). KT == 0: any K <= 32, broadcast per unit.
+// registers). KT == 0: any K <= 32, broadcast per unit. A unit is UN
+// consecutive 512-byte column blocks of one token, so each lane keeps
+// UN * K independent 16-byte loads in flight.
 template <int KT>
 __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const CombineArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    const int64_t n_cb = (a.row_bytes + kColBytes - 1) / kColBytes;
+    constexpr uint32_t kUnitBytes = kColBytes * kUnroll;
+    const int64_t n_cb = (a.row_bytes + kUnitBytes - 1) / kUnitBytes;
     const int64_t units = a.T * n_cb;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
@@ -82,7 +95,7 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
 
     for (int64_t u = u0; u < u1; ++u) {
         const int64_t t = u / n_cb;
-        const uint32_t col = static_cast<uint32_t>(u - t * n_cb) * kColBytes + lane * 16u;
+        const uint32_t col0 = static_cast<uint32_t>(u - t * n_cb) * kUnitBytes + lane * 16u;
         if (t != tok) {
             tok = t;
             int32_t s = lane < K ? __ldg(a.slot + t * K + lane) : -1;
@@ -103,29 +116,45 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
                 }
             }
         }
-        float acc[8];
+        float acc[kUnroll][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        const bool in_row = col < a.row_bytes;
+        for (int j = 0; j < kUnroll; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
+        bool in_row[kUnroll];
+#pragma unroll
+        for (int j = 0; j < kUnroll; ++j) in_row[j] = col0 + j * kColBytes < a.row_bytes;
         if (KT > 0) {
-            uint4 v[KR];
+            uint4 v[kUnroll][KR];
 #pragma unroll
-            for (int k = 0; k < KR; ++k) v[k] = make_uint4(0u, 0u, 0u, 0u);
+            for (int j = 0; j < kUnroll; ++j)
+#pragma unroll
+                for (int k = 0; k < KR; ++k) v[j][k] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int k = 0; k < KR; ++k)
-                if (on[k] && in_row) v[k] = ld_expert(rowp[k] + col);
 #pragma unroll
-            for (int k = 0; k < KR; ++k)
-                if (on[k] && in_row) fma8(acc, wk[k], v[k]);
+                for (int j = 0; j < kUnroll; ++j)
+                    if (on[k] && in_row[j]) v[j][k] = ld_expert(rowp[k] + col0 + j * kColBytes);
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j)
+#pragma unroll
+                for (int k = 0; k < KR; ++k)
+                    if (on[k] && in_row[j]) fma8(acc[j], wk[k], v[j][k]);
         } else {
             for (int k = 0; k < K; ++k) {
                 const int32_t sk = __shfl_sync(kFullMask, s_lane, k);
                 const float w = __shfl_sync(kFullMask, w_lane, k);
-                if (sk >= 0 && in_row)
-                    fma8(acc, w, ld_expert(a.expert_out + static_cast<int64_t>(sk) * a.row_bytes + col));
+                if (sk < 0) continue;
+                const uint8_t* row = a.expert_out + static_cast<int64_t>(sk) * a.row_bytes;
+#pragma unroll
+                for (int j = 0; j < kUnroll; ++j)
+                    if (in_row[j]) fma8(acc[j], w, ld_expert(row + col0 + j * kColBytes));
             }
         }
-        if (in_row) st_v4(a.y + t * static_cast<int64_t>(a.row_bytes) + col, round8(acc));
+        uint8_t* yrow = a.y + t * static_cast<int64_t>(a.row_bytes);
+#pragma unroll
+        for (int j = 0; j < kUnroll; ++j)
+            if (in_row[j]) st_v4(yrow + col0 + j * kColBytes, round8(acc[j]));
     }
 }
 
@@ -142,7 +171,7 @@ cudaError_t launch_k(const CombineArgs& a, int grid, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t stream) {
-    const int64_t n_cb = (a.row_bytes + kColBytes - 1) / kColBytes;
+    const int64_t n_cb = (a.row_bytes + kColBytes * kUnroll - 1) / (kColBytes * kUnroll);
     const int64_t units = a.T * n_cb;
     const int64_t warps_per_cta = kCombineThreads / 32;
     const int64_t ctas_needed = (units + warps_per_cta - 1) / warps_per_cta;

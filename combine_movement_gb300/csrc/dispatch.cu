@@ -32,8 +32,19 @@
 namespace ep {
 namespace {
 
+// Build-time shape of the ring (defaults are the tuned values).
+#ifndef EP_DISPATCH_WARPS
+#define EP_DISPATCH_WARPS 8
+#endif
+#ifndef EP_DISPATCH_STAGES
+#define EP_DISPATCH_STAGES 4
+#endif
+#ifndef EP_DISPATCH_PREFETCH
+#define EP_DISPATCH_PREFETCH 2
+#endif
+
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
-constexpr int kDispatchWarps = 8;
+constexpr int kDispatchWarps = EP_DISPATCH_WARPS;
 
 // Bytes reserved in front of the stages for the mbarriers (8 B per stage per
 // warp), rounded up so every stage starts 128-byte aligned.
@@ -154,9 +165,9 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1) dispatch_kernel(const 
     if (leader) bulk_wait<0>();
 }
 
-// Ring shapes compiled in: (stages, loads in flight ahead).
-constexpr int kStages = 4;
-constexpr int kPrefetch = 2;
+// Ring shape compiled in: stages per warp, loads in flight ahead.
+constexpr int kStages = EP_DISPATCH_STAGES;
+constexpr int kPrefetch = EP_DISPATCH_PREFETCH;
 
 }  // namespace
 

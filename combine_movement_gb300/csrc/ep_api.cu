@@ -61,6 +61,23 @@ int sms_in_effect(int sm_count) {
 
 ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 
+// Which combine kernel runs: the direct 16-byte gather (0), the bulk-copy
+// staged ring (1), or the ring only at budgets of at most
+// EP_COMBINE_TMA_MAX_SMS SMs (2). Both give identical results.
+#ifndef EP_COMBINE_MODE
+#define EP_COMBINE_MODE 0
+#endif
+#ifndef EP_COMBINE_TMA_MAX_SMS
+#define EP_COMBINE_TMA_MAX_SMS 64
+#endif
+
+bool use_combine_tma(int K, int num_sms) {
+    if (!ep::combine_tma_supported(K)) return false;
+    if (EP_COMBINE_MODE == 1) return true;
+    if (EP_COMBINE_MODE == 2) return num_sms <= EP_COMBINE_TMA_MAX_SMS;
+    return false;
+}
+
 }  // namespace
 
 extern "C" {
@@ -174,8 +191,10 @@ ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv, const int32
     a.K = K;
     a.y = reinterpret_cast<uint8_t*>(y);
     a.status = status;
-    return from_cuda(
-        ep::launch_combine(a, sms_in_effect(sm_count), static_cast<cudaStream_t>(stream)));
+    const int n = sms_in_effect(sm_count);
+    if (use_combine_tma(K, n))
+        return from_cuda(ep::launch_combine_tma(a, n, smem_optin, static_cast<cudaStream_t>(stream)));
+    return from_cuda(ep::launch_combine(a, n, static_cast<cudaStream_t>(stream)));
 }
 
 ep_status_t ep_get_status(const int32_t* status, void* stream) {

@@ -68,6 +68,12 @@ struct CombineArgs {
 
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t stream);
 
+// Combine with the expert rows staged through a per-warp bulk-copy ring
+// (combine_tma.cu); K <= 8 only.
+bool combine_tma_supported(int K);
+cudaError_t launch_combine_tma(const CombineArgs& a, int num_sms, int smem_optin,
+                               cudaStream_t stream);
+
 // Dynamic shared memory that makes a CTA the only one resident on its SM
 // (more than half of an SM's shared memory), so a grid of n CTAs occupies
 // exactly n SMs.

@@ -118,6 +118,16 @@ def ep_layout_workspace_bytes(T: int, K: int, E: int) -> int:
     return int(lib.ep_layout_workspace_bytes(T, K, E))
 
 
+def layout_launches(T: int, K: int, E: int) -> int:
+    """Kernel launches one ep_get_dispatch_layout call makes for these sizes:
+    one fused launch when no workspace is needed, else a tile and a finish
+    launch (three, with a separate scan, for very large tables)."""
+    nbytes = ep_layout_workspace_bytes(T, K, E)
+    if nbytes == 0:
+        return 1
+    return 2 if nbytes // 4 // E <= 512 else 3
+
+
 def ep_status_string(code: int) -> str:
     return lib.ep_status_string(int(code)).decode()
 
