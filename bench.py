@@ -175,7 +175,7 @@ class Step:
         self.b.x.copy_(inp.x)
         self.b.idx.copy_(inp.topk_idx)
         self.b.w.copy_(inp.topk_w)
-        self.layout_launches = ep.layout_launches(self.T, self.K, self.E)
+        self.layout_launches = ep.ep_layout_launches(self.T, self.K, self.E)
         # the experts between dispatch and combine are a fixed stand-in
         self.layout(self.b)
         self.dispatch(self.b)

@@ -8,9 +8,9 @@
 // at +0.0f, one fused multiply-add per k in ascending k (entries with slot < 0
 // skipped), one bf16 round-to-nearest-even per output element.
 //
-// Mapping: persistent grid of one CTA per SM (the SM budget). A unit is
-// EP_COMBINE_UNROLL 512-byte column blocks of one token row (a block is 32
-// lanes x 16 bytes); every warp
+// Mapping: persistent grid of one CTA per SM (the SM budget). A unit is one
+// or two 512-byte column blocks of one token row (a block is 32 lanes x 16
+// bytes); every warp
 // takes a contiguous, equal range of units, so the load is balanced to within
 // one unit whatever T and the budget. For each token the warp reads slot and
 // weight once (lanes k < K) and broadcasts them with warp shuffles; each lane
@@ -27,17 +27,27 @@
 namespace ep {
 namespace {
 
-// Build-time shape (defaults are the tuned values).
-#ifndef EP_COMBINE_THREADS
-#define EP_COMBINE_THREADS 512
+// Two compiled shapes (threads per CTA, column blocks per unit), chosen by
+// the SM budget: with many SMs, fewer threads with two blocks in flight each
+// win; with few SMs, more threads (more loads in flight per SM) win.
+#ifndef EP_COMBINE_WIDE_THREADS
+#define EP_COMBINE_WIDE_THREADS 384
 #endif
-#ifndef EP_COMBINE_UNROLL
-#define EP_COMBINE_UNROLL 2
+#ifndef EP_COMBINE_WIDE_UNROLL
+#define EP_COMBINE_WIDE_UNROLL 2
+#endif
+#ifndef EP_COMBINE_NARROW_THREADS
+#define EP_COMBINE_NARROW_THREADS 768
+#endif
+#ifndef EP_COMBINE_NARROW_UNROLL
+#define EP_COMBINE_NARROW_UNROLL 1
+#endif
+// Budgets of at least this many SMs use the wide shape.
+#ifndef EP_COMBINE_WIDE_MIN_SMS
+#define EP_COMBINE_WIDE_MIN_SMS 96
 #endif
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
-constexpr int kCombineThreads = EP_COMBINE_THREADS;
-constexpr int kUnroll = EP_COMBINE_UNROLL;
 constexpr uint32_t kColBytes = 512;  // row bytes one warp covers per column block
 
 __device__ __forceinline__ uint4 ld_expert(const uint8_t* p) {
@@ -72,8 +82,10 @@ __device__ __forceinline__ uint4 round8(const float (&acc)[8]) {
 // registers). KT == 0: any K <= 32, broadcast per unit. A unit is UN
 // consecutive 512-byte column blocks of one token, so each lane keeps
 // UN * K independent 16-byte loads in flight.
-template <int KT>
-__global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const CombineArgs a) {
+template <int KT, int kThreads, int kUnroll>
+__global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs a) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     constexpr uint32_t kUnitBytes = kColBytes * kUnroll;
@@ -158,35 +170,41 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
     }
 }
 
-template <int KT>
-cudaError_t launch_k(const CombineArgs& a, int grid, cudaStream_t stream) {
-    auto kern = combine_kernel<KT>;
+template <int KT, int kThreads, int kUnroll>
+cudaError_t launch_shape(const CombineArgs& a, int num_sms, cudaStream_t stream) {
+    constexpr uint32_t kUnitBytes = kColBytes * kUnroll;
+    const int64_t units = a.T * ((a.row_bytes + kUnitBytes - 1) / kUnitBytes);
+    const int64_t warps_per_cta = kThreads / 32;
+    const int64_t ctas_needed = (units + warps_per_cta - 1) / warps_per_cta;
+    const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
+    if (grid <= 0) return cudaSuccess;
+    auto kern = combine_kernel<KT, kThreads, kUnroll>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kExclusiveSmem));
     if (err != cudaSuccess) return err;
-    kern<<<grid, kCombineThreads, kExclusiveSmem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kern, grid, kThreads, kExclusiveSmem, stream, a);
+}
+
+template <int KT>
+cudaError_t launch_k(const CombineArgs& a, int num_sms, cudaStream_t stream) {
+    if (num_sms >= EP_COMBINE_WIDE_MIN_SMS)
+        return launch_shape<KT, EP_COMBINE_WIDE_THREADS, EP_COMBINE_WIDE_UNROLL>(a, num_sms, stream);
+    return launch_shape<KT, EP_COMBINE_NARROW_THREADS, EP_COMBINE_NARROW_UNROLL>(a, num_sms, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t stream) {
-    const int64_t n_cb = (a.row_bytes + kColBytes * kUnroll - 1) / (kColBytes * kUnroll);
-    const int64_t units = a.T * n_cb;
-    const int64_t warps_per_cta = kCombineThreads / 32;
-    const int64_t ctas_needed = (units + warps_per_cta - 1) / warps_per_cta;
-    const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
-    if (grid <= 0) return cudaSuccess;
     switch (a.K) {
-        case 1: return launch_k<1>(a, grid, stream);
-        case 2: return launch_k<2>(a, grid, stream);
-        case 3: return launch_k<3>(a, grid, stream);
-        case 4: return launch_k<4>(a, grid, stream);
-        case 5: return launch_k<5>(a, grid, stream);
-        case 6: return launch_k<6>(a, grid, stream);
-        case 7: return launch_k<7>(a, grid, stream);
-        case 8: return launch_k<8>(a, grid, stream);
-        default: return launch_k<0>(a, grid, stream);
+        case 1: return launch_k<1>(a, num_sms, stream);
+        case 2: return launch_k<2>(a, num_sms, stream);
+        case 3: return launch_k<3>(a, num_sms, stream);
+        case 4: return launch_k<4>(a, num_sms, stream);
+        case 5: return launch_k<5>(a, num_sms, stream);
+        case 6: return launch_k<6>(a, num_sms, stream);
+        case 7: return launch_k<7>(a, num_sms, stream);
+        case 8: return launch_k<8>(a, num_sms, stream);
+        default: return launch_k<0>(a, num_sms, stream);
     }
 }
 

@@ -94,6 +94,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) combine_tma_kernel(const Co
         fence_mbar_init();
     }
     __syncwarp();
+    griddep_wait();
+    griddep_launch_dependents();
 
     const int64_t n_c = (a.row_bytes + kChunk - 1) / kChunk;
     const int64_t units = a.T * n_c;
@@ -231,8 +233,7 @@ cudaError_t launch_kt(const CombineArgs& a, int num_sms, int smem_optin, cudaStr
     const int64_t ctas_needed = (units + warps - 1) / warps;
     const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, warps * 32, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kern, grid, warps * 32, smem, stream, a);
 }
 
 }  // namespace

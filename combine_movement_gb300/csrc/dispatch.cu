@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1) dispatch_kernel(const 
         fence_mbar_init();
     }
     __syncwarp();
+    griddep_wait();
+    griddep_launch_dependents();
 
     const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
@@ -165,6 +167,69 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1) dispatch_kernel(const 
     if (leader) bulk_wait<0>();
 }
 
+// ---- ablation: the same copy through the load/store units ---------------------
+// Every lane moves 16-byte vectors with plain ld.global / st.global: a warp
+// loads kLsuBlocks 512-byte column blocks of a row into registers and stores
+// them to each of the K receive rows. This is the register-staged copy the
+// pages contrast TMA with ("How DeepEP Utilizes TMA Instructions for Minimal
+// SM Usage on Hopper GPUs", Summary and FAQ: the UNROLLED_WARP_COPY path of
+// pre-Hopper GPUs; TMA study note, history of copying). Built only with
+// EP_DISPATCH_MODE=1, for measuring what the bulk-copy path saves; it moves
+// the rows only (no recv_w / recv_src).
+#ifndef EP_DISPATCH_MODE
+#define EP_DISPATCH_MODE 0
+#endif
+#ifndef EP_LSU_THREADS
+#define EP_LSU_THREADS 512
+#endif
+#ifndef EP_LSU_BLOCKS
+#define EP_LSU_BLOCKS 4
+#endif
+constexpr int kLsuThreads = EP_LSU_THREADS;
+constexpr int kLsuBlocks = EP_LSU_BLOCKS;
+
+__global__ void __launch_bounds__(kLsuThreads, 1) dispatch_lsu_kernel(const DispatchArgs a) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    constexpr uint32_t kUnit = 512u * kLsuBlocks;
+    const int64_t n_cb = (a.row_bytes + kUnit - 1) / kUnit;
+    const int64_t units = a.T * n_cb;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
+    const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
+    const int64_t u0 = units * gw / nw_total, u1 = units * (gw + 1) / nw_total;
+    int64_t tok = -1;
+    int32_t s_lane = -1;
+    for (int64_t u = u0; u < u1; ++u) {
+        const int64_t t = u / n_cb;
+        const uint32_t col0 = static_cast<uint32_t>(u - t * n_cb) * kUnit + lane * 16u;
+        if (t != tok) {
+            tok = t;
+            s_lane = lane < a.K ? __ldg(a.slot + t * a.K + lane) : -1;
+        }
+        uint4 v[kLsuBlocks];
+        const uint8_t* src = a.x + t * static_cast<int64_t>(a.row_bytes);
+#pragma unroll
+        for (int b = 0; b < kLsuBlocks; ++b) {
+            v[b] = make_uint4(0u, 0u, 0u, 0u);
+            if (col0 + b * 512u < a.row_bytes) v[b] = ld_nc_v4(src + col0 + b * 512u);
+        }
+        for (int k = 0; k < a.K; ++k) {
+            const int32_t d = __shfl_sync(kFullMask, s_lane, k);
+            if (d < 0) continue;
+            if (d >= a.num_recv) {
+                if (lane == 0) set_status(a.status, EP_ERR_BAD_SLOT);
+                continue;
+            }
+            uint8_t* dst = a.recv_x + static_cast<int64_t>(d) * a.row_bytes;
+#pragma unroll
+            for (int b = 0; b < kLsuBlocks; ++b)
+                if (col0 + b * 512u < a.row_bytes) st_v4(dst + col0 + b * 512u, v[b]);
+        }
+    }
+}
+
 // Ring shape compiled in: stages per warp, loads in flight ahead.
 constexpr int kStages = EP_DISPATCH_STAGES;
 constexpr int kPrefetch = EP_DISPATCH_PREFETCH;
@@ -174,6 +239,13 @@ constexpr int kPrefetch = EP_DISPATCH_PREFETCH;
 cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, int smem_optin,
                             cudaStream_t stream) {
     (void)smem_optin;
+    if (EP_DISPATCH_MODE == 1) {
+        cudaError_t e = cudaFuncSetAttribute(dispatch_lsu_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kExclusiveSmem));
+        if (e != cudaSuccess) return e;
+        return launch_dependent(dispatch_lsu_kernel, num_sms, kLsuThreads, kExclusiveSmem, stream, a);
+    }
     const size_t smem = static_cast<size_t>(barrier_region(kStages, kDispatchWarps)) +
                         static_cast<size_t>(kDispatchWarps) * kStages * a.stage_bytes;
     const size_t request = smem < kExclusiveSmem ? kExclusiveSmem : smem;
@@ -186,8 +258,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, int smem_optin,
     int64_t ctas_needed = (units + kDispatchWarps - 1) / kDispatchWarps;
     const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, kDispatchWarps * 32, request, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kern, grid, kDispatchWarps * 32, request, stream, a);
 }
 
 // Stage size the host plans rows with: the per-warp slice split into the

@@ -101,6 +101,13 @@ size_t ep_layout_workspace_bytes(int64_t T, int K, int E) {
     return ep::plan_layout(T * K, E).workspace_bytes;
 }
 
+int ep_layout_launches(int64_t T, int K, int E) {
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return -1;
+    const ep::LayoutPlan p = ep::plan_layout(T * K, E);
+    if (p.num_tiles == 1 || p.coop) return 1;
+    return p.num_tiles <= 512 ? 2 : 3;
+}
+
 ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, int E,
                                    int32_t* counts, int32_t* offsets, int32_t* slot,
                                    void* workspace, size_t workspace_bytes, int32_t* status,
@@ -116,11 +123,10 @@ ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, in
     const ep::LayoutPlan plan = ep::plan_layout(T * K, E);
     if (plan.workspace_bytes > 0) {
         if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return EP_ERR_WORKSPACE;
-        if (!aligned(workspace, 4)) return EP_ERR_INVALID;
+        if (!aligned(workspace, 16)) return EP_ERR_INVALID;
     }
-    return from_cuda(ep::launch_layout(topk_idx, T * K, E, counts, offsets, slot,
-                                       static_cast<int32_t*>(workspace), plan, status,
-                                       static_cast<cudaStream_t>(stream)));
+    return from_cuda(ep::launch_layout(topk_idx, T * K, E, counts, offsets, slot, workspace, plan,
+                                       status, static_cast<cudaStream_t>(stream)));
 }
 
 ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const int32_t* slot,

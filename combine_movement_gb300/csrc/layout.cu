@@ -13,18 +13,22 @@
 //   1. tile kernel (one block per tile): loads the tile's ids once, counts
 //      them per warp (warp match), scans across warps and assigns every entry
 //      its rank among the tile's entries of the same expert, in entry order;
-//      writes the tile's per-expert counts to tile_counts[e][tile] and the
+//      writes the tile's per-expert counts to tile_counts[tile][e] and the
 //      packed (rank, expert) into slot.
 //   2. finish kernel (one block per tile): computes, from the small
-//      [E][tiles] array, each expert's first row and the rows taken by
+//      [tiles][E] table, each expert's first row and the rows taken by
 //      earlier tiles (every block does this itself, saving a launch), then
 //      rewrites each packed entry as its final slot; block 0 writes counts
 //      and offsets. Very large tables scan once in a separate one-block
 //      kernel instead.
 // A table that fits one tile takes a single fused launch. No position
-// depends on the order of concurrent operations (there are no atomics; the
-// per-warp counts are owned by their warp), so the result is deterministic.
+// depends on the order of concurrent operations: per-warp counts are owned
+// by their warp, and the only atomics are integer sums (order-free), so the
+// result is deterministic.
 #include <cuda_runtime.h>
+#include <unistd.h>
+
+#include <chrono>
 
 #include "../../include/ep.h"
 #include "kernels.cuh"
@@ -38,6 +42,7 @@ constexpr size_t kRunSmemBudget = 64 * 1024;  // per-warp expert counters of the
 constexpr int kMaxRounds = 8;                 // 32-entry rounds per warp per tile, at most
 constexpr int kTargetTiles = 128;             // tiles to aim for before rounds grow
 constexpr int kMaxRedundantTiles = 512;       // above this, one block scans for everyone
+constexpr int kCoopMaxTiles = 128;            // tables of at most this many tiles: one launch
 constexpr int kScanThreads = 1024;
 constexpr int kFinishThreads = 512;
 constexpr int kExpertBits = 12;               // packed entry: (rank << 12) | expert, E <= 4096
@@ -89,6 +94,48 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t* total) {
     return out;
 }
 
+// Lanes of the warp whose key equals this lane's key (all invalid lanes,
+// key -1, form one group). Built from one ballot per key bit: a handful of
+// single-cycle votes instead of a warp match.
+__device__ __forceinline__ uint32_t peers_of(int key, int key_bits) {
+    const uint32_t valid = __ballot_sync(kFullMask, key >= 0);
+    uint32_t m = key >= 0 ? valid : ~valid;
+    for (int b = 0; b < key_bits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const uint32_t ones = __ballot_sync(kFullMask, bit);
+        m &= bit ? ones : ~ones;
+    }
+    return m;
+}
+
+// Bits needed for expert ids 0..E-1.
+__device__ __forceinline__ int key_bits_for(int E) { return E > 1 ? 32 - __clz(E - 1) : 0; }
+
+// Exclusive scan across the block's warps of the per-warp counts
+// run[w][e], one expert per thread (in place); writes the tile total of
+// each expert to out[e * stride]. Loads are batched 8 warps at a
+// time so the chain does not wait on shared memory once per warp.
+__device__ __forceinline__ void scan_across_warps(int32_t* run, int E, int nwarps,
+                                                  int32_t* out, int64_t stride) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t acc = 0;
+        for (int w0 = 0; w0 < nwarps; w0 += 8) {
+            int32_t c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                c[u] = w0 + u < nwarps ? run[static_cast<int64_t>(w0 + u) * E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (w0 + u < nwarps) {
+                    run[static_cast<int64_t>(w0 + u) * E + e] = acc;
+                    acc += c[u];
+                }
+            }
+        }
+        out[static_cast<int64_t>(e) * stride] = acc;
+    }
+}
+
 // ---- tile kernel: per-warp counts, per-tile ranks ----------------------------
 // Every warp owns `rounds` consecutive 32-entry rounds of its tile; all of
 // its routing ids are loaded up front (one memory latency, not one per
@@ -97,19 +144,22 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t* total) {
 // per-warp starting ranks; pass B hands out ranks in entry order.
 //  FUSED (the whole table is one tile): the block also scans across experts
 //    and writes counts, offsets and final slots.
-//  otherwise: writes the tile's per-expert counts to tile_counts[e][tile]
+//  otherwise: writes the tile's per-expert counts to tile_counts[tile][e]
 //    and, per entry, (rank within the tile << 12) | expert into slot, which
 //    layout_finish_kernel turns into the final slot.
 template <bool FUSED>
-__global__ void layout_tile_kernel(const int64_t* __restrict__ idx, int64_t N, int E, int rounds,
+__global__ void __launch_bounds__(1024) layout_tile_kernel(const int64_t* __restrict__ idx, int64_t N, int E, int rounds,
                                    int num_tiles, int32_t* __restrict__ tile_counts,
                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                    int32_t* __restrict__ slot, int32_t* status) {
     extern __shared__ int32_t run[];  // [warps][E]
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     const int64_t tile = static_cast<int64_t>(nwarps) * 32 * rounds;
     const int64_t wbase = tile * blockIdx.x + static_cast<int64_t>(warp) * 32 * rounds;
+    const int kbits = key_bits_for(E);
 
     int key[kMaxRounds];
     bool bad = false;
@@ -129,7 +179,7 @@ __global__ void layout_tile_kernel(const int64_t* __restrict__ idx, int64_t N, i
 #pragma unroll
     for (int r = 0; r < kMaxRounds; ++r) {
         if (r < rounds) {
-            const uint32_t peers = __match_any_sync(kFullMask, key[r]);
+            const uint32_t peers = peers_of(key[r], kbits);
             if (key[r] >= 0 && lane == __ffs(peers) - 1) my[key[r]] += __popc(peers);
             __syncwarp();
         }
@@ -159,15 +209,7 @@ __global__ void layout_tile_kernel(const int64_t* __restrict__ idx, int64_t N, i
         }
         if (threadIdx.x == 0) offsets[E] = static_cast<int32_t>(total);
     } else {
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
-            int32_t acc = 0;
-            for (int w = 0; w < nwarps; ++w) {
-                const int32_t c = run[static_cast<int64_t>(w) * E + e];
-                run[static_cast<int64_t>(w) * E + e] = acc;
-                acc += c;
-            }
-            tile_counts[static_cast<int64_t>(e) * num_tiles + blockIdx.x] = acc;
-        }
+        scan_across_warps(run, E, nwarps, tile_counts + static_cast<int64_t>(blockIdx.x) * E, 1);
     }
     __syncthreads();
 
@@ -176,7 +218,7 @@ __global__ void layout_tile_kernel(const int64_t* __restrict__ idx, int64_t N, i
         if (r < rounds) {
             const int64_t i = wbase + r * 32 + lane;
             const int k = key[r];
-            const uint32_t peers = __match_any_sync(kFullMask, k);
+            const uint32_t peers = peers_of(k, kbits);
             if (i < N) {
                 if (k >= 0) {
                     const int32_t rank = my[k] + __popc(peers & lanemask_lt());
@@ -193,28 +235,34 @@ __global__ void layout_tile_kernel(const int64_t* __restrict__ idx, int64_t N, i
 }
 
 // ---- scan over (expert, tile), one block (large tables only) -----------------
-// In place: tile_counts[e][b] becomes the first receive row of expert e's
-// entries in tile b; also writes counts and offsets.
+// In place over the tile-major table: tile_counts[b][e] becomes the first
+// receive row of expert e's entries in tile b (experts in order, tiles in
+// order within an expert); also writes counts and offsets.
 __global__ void __launch_bounds__(kScanThreads) layout_scan_kernel(
     int32_t* __restrict__ tile_counts, int num_tiles, int E, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t M = static_cast<int64_t>(E) * num_tiles;
     const int64_t per = (M + blockDim.x - 1) / blockDim.x;
     const int64_t lo = min(M, per * threadIdx.x), hi = min(M, lo + per);
+    // position q of the expert-major order lives at [q % tiles][q / tiles]
+    auto at = [&](int64_t q) -> int32_t& {
+        return tile_counts[(q % num_tiles) * E + q / num_tiles];
+    };
     int64_t local = 0;
-    for (int64_t i = lo; i < hi; ++i) local += tile_counts[i];
+    for (int64_t q = lo; q < hi; ++q) local += at(q);
     int64_t total;
     int64_t run = block_exclusive_scan(local, &total);
-    for (int64_t i = lo; i < hi; ++i) {
-        const int32_t c = tile_counts[i];
-        tile_counts[i] = static_cast<int32_t>(run);
+    for (int64_t q = lo; q < hi; ++q) {
+        const int32_t c = at(q);
+        at(q) = static_cast<int32_t>(run);
         run += c;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int32_t first = tile_counts[static_cast<int64_t>(e) * num_tiles];
-        const int32_t next = (e + 1 < E) ? tile_counts[static_cast<int64_t>(e + 1) * num_tiles]
-                                         : static_cast<int32_t>(total);
+        const int32_t first = tile_counts[e];
+        const int32_t next = (e + 1 < E) ? tile_counts[e + 1] : static_cast<int32_t>(total);
         offsets[e] = first;
         counts[e] = next - first;
     }
@@ -224,7 +272,7 @@ __global__ void __launch_bounds__(kScanThreads) layout_scan_kernel(
 // ---- finish kernel: final slots ------------------------------------------------
 // One block per tile. Unless PRESCANNED, every block computes the prefix it
 // needs itself (expert totals and the counts of earlier tiles, read from the
-// small [E][tiles] array; one scan across experts), which saves a launch;
+// small [tiles][E] table; one scan across experts), which saves a launch;
 // block 0 also writes counts and offsets. Then each packed entry becomes
 // base[expert] + rank.
 template <bool PRESCANNED>
@@ -232,26 +280,43 @@ __global__ void __launch_bounds__(kFinishThreads) layout_finish_kernel(
     const int32_t* __restrict__ tile_counts, int num_tiles, int E, int64_t N, int64_t tile,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot) {
     extern __shared__ int32_t base[];  // [E] (+ [E] of totals when !PRESCANNED)
+    griddep_wait();
+    griddep_launch_dependents();
     if (PRESCANNED) {
         for (int e = threadIdx.x; e < E; e += blockDim.x)
-            base[e] = tile_counts[static_cast<int64_t>(e) * num_tiles + blockIdx.x];
+            base[e] = tile_counts[static_cast<int64_t>(blockIdx.x) * E + e];
     } else {
         int32_t* tot = base + E;
+        for (int e = threadIdx.x; e < E; e += blockDim.x) tot[e] = base[e] = 0;
+        __syncthreads();
+        // Expert totals and the rows taken by earlier tiles: one coalesced
+        // pass over the [tiles][E] counts, loads batched ahead of the
+        // (order-free) integer shared-memory adds.
+        const int64_t M = static_cast<int64_t>(E) * num_tiles;
+        constexpr int kBatch = 8;
+        for (int64_t f0 = threadIdx.x; f0 < M; f0 += static_cast<int64_t>(blockDim.x) * kBatch) {
+            int32_t c[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t f = f0 + static_cast<int64_t>(u) * blockDim.x;
+                c[u] = f < M ? __ldg(tile_counts + f) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t f = f0 + static_cast<int64_t>(u) * blockDim.x;
+                if (f < M && c[u] != 0) {
+                    const int b = static_cast<int>(f / E);
+                    const int e = static_cast<int>(f - static_cast<int64_t>(b) * E);
+                    atomicAdd(&tot[e], c[u]);
+                    if (b < static_cast<int>(blockIdx.x)) atomicAdd(&base[e], c[u]);
+                }
+            }
+        }
+        __syncthreads();
         const int per = (E + blockDim.x - 1) / blockDim.x;
         const int e0 = min(E, per * static_cast<int>(threadIdx.x)), e1 = min(E, e0 + per);
         int64_t local = 0;
-        for (int e = e0; e < e1; ++e) {
-            const int32_t* row = tile_counts + static_cast<int64_t>(e) * num_tiles;
-            int32_t t = 0, before = 0;
-            for (int b = 0; b < num_tiles; ++b) {
-                const int32_t c = __ldg(row + b);
-                t += c;
-                before += b < static_cast<int>(blockIdx.x) ? c : 0;
-            }
-            tot[e] = t;
-            base[e] = before;
-            local += t;
-        }
+        for (int e = e0; e < e1; ++e) local += tot[e];
         int64_t total;
         int64_t off = block_exclusive_scan(local, &total);
         for (int e = e0; e < e1; ++e) {
@@ -273,6 +338,173 @@ __global__ void __launch_bounds__(kFinishThreads) layout_finish_kernel(
     }
 }
 
+// ---- single-launch layout (cooperative grid) -----------------------------------
+// For tables of up to kCoopMaxTiles tiles, one cooperative launch does what
+// the tile and finish kernels do, with one grid-wide barrier in between:
+//   phase 1  per tile: ids, per-warp counts, ranks within the tile (kept in
+//            registers), the tile's per-expert counts to tile_counts[tile][e]
+//   phase 2  per tile: read the whole small [tiles][E] table (one coalesced,
+//            batched pass), giving each expert's total and the rows taken by
+//            earlier tiles; scan the totals across experts; write every
+//            entry's final slot once. Block 0 writes counts and offsets.
+// The barrier: each block publishes a 64-bit target value in its flag word
+// and waits (bounded in time) until every block's flag holds it. The target
+// is the generation word kept in the workspace plus one, under a per-process
+// salt in the upper half (its top bit set, so no stale pair of counts can
+// spell it); block 0 stores the new generation once every block has passed
+// the barrier (or, after a timed-out wait, the giving-up block does). So the
+// barrier words need no clearing between calls, and a replayed launch with
+// identical arguments still waits for fresh flags.
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// All blocks of the grid arrive and wait; false (in every thread of the
+// block) if some block's flag did not arrive within kWaitLimitNs.
+__device__ bool grid_barrier(uint64_t* flags, int nblocks, uint64_t target) {
+    __syncthreads();  // the block's writes precede thread 0's release (cumulative)
+    if (threadIdx.x == 0) st_release_u64(flags + blockIdx.x, target);
+    bool ok = true;
+    for (int b = threadIdx.x; b < nblocks && ok; b += blockDim.x) {
+        if (ld_acquire_u64(flags + b) == target) continue;
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire_u64(flags + b) != target) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                ok = false;
+                break;
+            }
+        }
+    }
+    return __syncthreads_and(ok) != 0;  // the acquires precede the block's reads
+}
+
+__global__ void __launch_bounds__(1024) layout_coop_kernel(const int64_t* __restrict__ idx, int64_t N, int E, int rounds,
+                                   uint64_t* sync, int32_t* tile_counts, uint32_t salt,
+                                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                   int32_t* __restrict__ slot, int32_t* status) {
+    extern __shared__ int32_t run[];  // [warps][E]; phase 2 reuses the first 2E words
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int nt = gridDim.x, tile_id = blockIdx.x;
+    const int64_t tile = static_cast<int64_t>(nwarps) * 32 * rounds;
+    const int64_t wbase = tile * tile_id + static_cast<int64_t>(warp) * 32 * rounds;
+    const int kbits = key_bits_for(E);
+
+    griddep_launch_dependents();  // all blocks are resident (cooperative launch)
+    // generation: read before the barrier, replaced after it
+    const uint64_t g = *reinterpret_cast<volatile uint64_t*>(sync);
+    const uint64_t g0 = (g >> 32) == salt ? g : (static_cast<uint64_t>(salt) << 32);
+    const uint64_t target = g0 + 1;
+
+    // phase 1 ------------------------------------------------------------
+    int key[kMaxRounds];
+    int32_t rank[kMaxRounds];
+    bool bad = false;
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+        key[r] = -1;
+        rank[r] = 0;
+        const int64_t i = wbase + r * 32 + lane;
+        if (r < rounds && i < N) {
+            const int64_t v = __ldg(idx + i);
+            key[r] = expert_key(v, E);
+            bad |= (key[r] < 0 && v != -1);
+        }
+    }
+    if (bad) set_status(status, EP_ERR_BAD_EXPERT);
+    int32_t* my = run + static_cast<int64_t>(warp) * E;
+    for (int e = lane; e < E; e += 32) my[e] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+        if (r < rounds) {
+            const uint32_t peers = peers_of(key[r], kbits);
+            if (key[r] >= 0 && lane == __ffs(peers) - 1) my[key[r]] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    scan_across_warps(run, E, nwarps, tile_counts + static_cast<int64_t>(tile_id) * E, 1);
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+        if (r < rounds) {
+            const int k = key[r];
+            const uint32_t peers = peers_of(k, kbits);
+            if (k >= 0) rank[r] = my[k] + __popc(peers & lanemask_lt());
+            __syncwarp();
+            if (k >= 0 && lane == __ffs(peers) - 1) my[k] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    if (!grid_barrier(sync + 1, nt, target)) {
+        // leave the generation past every flag this call may have published
+        if (threadIdx.x == 0) {
+            set_status(status, EP_ERR_TIMEOUT);
+            st_release_u64(sync, target);
+        }
+        return;
+    }
+    if (tile_id == 0 && threadIdx.x == 0) st_release_u64(sync, target);
+
+    // phase 2: per expert, its total and the rows of earlier tiles. Q threads
+    // share an expert (tiles q, q+Q, ...); all of a thread's loads are in
+    // flight at once; order-free integer adds combine the Q partial sums.
+    int32_t* tot = run;       // [E]
+    int32_t* base = run + E;  // [E]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) tot[e] = base[e] = 0;
+    __syncthreads();
+    {
+        const int Q = blockDim.x >= E ? static_cast<int>(blockDim.x) / E : 1;
+        for (int x = threadIdx.x; x < E * Q; x += blockDim.x) {
+            const int e = x % E, q = x / E;
+            int32_t t_sum = 0, b_sum = 0;
+            for (int t0 = q; t0 < nt; t0 += 16 * Q) {
+                int32_t c[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int t = t0 + u * Q;
+                    c[u] = t < nt ? __ldcg(tile_counts + static_cast<int64_t>(t) * E + e) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    t_sum += c[u];
+                    b_sum += (t0 + u * Q < tile_id) ? c[u] : 0;
+                }
+            }
+            if (t_sum != 0) atomicAdd(&tot[e], t_sum);
+            if (b_sum != 0) atomicAdd(&base[e], b_sum);
+        }
+    }
+    __syncthreads();
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, per * static_cast<int>(threadIdx.x)), e1 = min(E, e0 + per);
+    int64_t local = 0;
+    for (int e = e0; e < e1; ++e) local += tot[e];
+    int64_t total;
+    int64_t off = block_exclusive_scan(local, &total);
+    for (int e = e0; e < e1; ++e) {
+        if (tile_id == 0) {
+            offsets[e] = static_cast<int32_t>(off);
+            counts[e] = tot[e];
+        }
+        base[e] += static_cast<int32_t>(off);
+        off += tot[e];
+    }
+    if (tile_id == 0 && threadIdx.x == 0) offsets[E] = static_cast<int32_t>(total);
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+        const int64_t i = wbase + r * 32 + lane;
+        if (r < rounds && i < N) slot[i] = key[r] >= 0 ? base[key[r]] + rank[r] : -1;
+    }
+}
+
 }  // namespace
 
 LayoutPlan plan_layout(int64_t N, int E) {
@@ -291,39 +523,82 @@ LayoutPlan plan_layout(int64_t N, int E) {
     }
     p.tile = per_round * p.rounds;
     if (N > per_round * kMaxRounds) p.num_tiles = static_cast<int>((N + p.tile - 1) / p.tile);
-    p.workspace_bytes =
-        p.num_tiles > 1 ? sizeof(int32_t) * static_cast<size_t>(E) * p.num_tiles : 0;
     p.smem = sizeof(int32_t) * static_cast<size_t>(E) * warps;
+    p.coop = p.num_tiles > 1 && p.num_tiles <= kCoopMaxTiles;
+    if (p.num_tiles > 1) {
+        // [generation][flag x tiles] | tile_counts[tiles][E]
+        auto up16 = [](size_t v) { return (v + 15) & ~static_cast<size_t>(15); };
+        p.counts_off = up16(sizeof(uint64_t) * (1 + static_cast<size_t>(p.num_tiles)));
+        p.workspace_bytes = p.counts_off + sizeof(int32_t) * static_cast<size_t>(E) * p.num_tiles;
+    }
     return p;
 }
 
+namespace {
+// Per-process salt of the layout barriers' generation values (top bit set).
+uint32_t barrier_salt() {
+    static const uint32_t salt = [] {
+        const uint64_t t = static_cast<uint64_t>(
+            std::chrono::steady_clock::now().time_since_epoch().count());
+        const uint64_t h = (t ^ (static_cast<uint64_t>(getpid()) << 21)) * 0x9E3779B97F4A7C15ull;
+        return static_cast<uint32_t>(h >> 32) | 0x80000000u;
+    }();
+    return salt;
+}
+}  // namespace
+
 cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,
-                          int32_t* offsets, int32_t* slot, int32_t* tile_counts,
+                          int32_t* offsets, int32_t* slot, void* workspace,
                           const LayoutPlan& p, int32_t* status, cudaStream_t stream) {
     const int threads = p.warps * 32;
-    // The tile kernel's dynamic shared memory can exceed the default 48 KB
-    // (it also holds a few static words for the block scan).
-    cudaError_t err = cudaFuncSetAttribute(
-        p.num_tiles == 1 ? layout_tile_kernel<true> : layout_tile_kernel<false>,
-        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kRunSmemBudget));
-    if (err != cudaSuccess) return err;
     if (p.num_tiles == 1) {
-        layout_tile_kernel<true><<<1, threads, p.smem, stream>>>(idx, N, E, p.rounds, 1, nullptr,
-                                                                 counts, offsets, slot, status);
-        return cudaGetLastError();
+        // The tile kernel's dynamic shared memory can exceed the default 48 KB
+        // (it also holds a few static words for the block scan).
+        cudaError_t err = cudaFuncSetAttribute(layout_tile_kernel<true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kRunSmemBudget));
+        if (err != cudaSuccess) return err;
+        return launch_dependent(layout_tile_kernel<true>, 1, threads, p.smem, stream, idx, N, E,
+                                p.rounds, 1, static_cast<int32_t*>(nullptr), counts, offsets,
+                                slot, status);
     }
-    layout_tile_kernel<false><<<p.num_tiles, threads, p.smem, stream>>>(
-        idx, N, E, p.rounds, p.num_tiles, tile_counts, counts, offsets, slot, status);
-    if (p.num_tiles <= kMaxRedundantTiles) {
-        layout_finish_kernel<false><<<p.num_tiles, kFinishThreads, 2 * sizeof(int32_t) * E, stream>>>(
-            tile_counts, p.num_tiles, E, N, p.tile, counts, offsets, slot);
-    } else {
-        layout_scan_kernel<<<1, kScanThreads, 0, stream>>>(tile_counts, p.num_tiles, E, counts,
-                                                           offsets);
-        layout_finish_kernel<true><<<p.num_tiles, kFinishThreads, sizeof(int32_t) * E, stream>>>(
-            tile_counts, p.num_tiles, E, N, p.tile, counts, offsets, slot);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint64_t* sync = reinterpret_cast<uint64_t*>(ws);
+    int32_t* tile_counts = reinterpret_cast<int32_t*>(ws + p.counts_off);
+    if (p.coop) {
+        cudaError_t err = cudaFuncSetAttribute(layout_coop_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kRunSmemBudget));
+        if (err != cudaSuccess) return err;
+        int rounds = p.rounds;
+        uint32_t salt = barrier_salt();
+        void* args[] = {(void*)&idx,  (void*)&N,      (void*)&E,       (void*)&rounds,
+                        (void*)&sync, (void*)&tile_counts, (void*)&salt, (void*)&counts,
+                        (void*)&offsets, (void*)&slot, (void*)&status};
+        err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(layout_coop_kernel),
+                                          dim3(p.num_tiles), dim3(threads), args, p.smem, stream);
+        if (err == cudaSuccess) return cudaSuccess;
+        if (err != cudaErrorCooperativeLaunchTooLarge) return err;
+        (void)cudaGetLastError();  // too many tiles to be resident at once: two launches instead
     }
-    return cudaGetLastError();
+    cudaError_t err = cudaFuncSetAttribute(layout_tile_kernel<false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kRunSmemBudget));
+    if (err != cudaSuccess) return err;
+    err = launch_dependent(layout_tile_kernel<false>, p.num_tiles, threads, p.smem, stream, idx, N,
+                           E, p.rounds, p.num_tiles, tile_counts, counts, offsets, slot, status);
+    if (err != cudaSuccess) return err;
+    if (p.num_tiles <= kMaxRedundantTiles)
+        return launch_dependent(layout_finish_kernel<false>, p.num_tiles, kFinishThreads,
+                                2 * sizeof(int32_t) * E, stream,
+                                static_cast<const int32_t*>(tile_counts), p.num_tiles, E, N, p.tile,
+                                counts, offsets, slot);
+    err = launch_dependent(layout_scan_kernel, 1, kScanThreads, 0, stream, tile_counts,
+                           p.num_tiles, E, counts, offsets);
+    if (err != cudaSuccess) return err;
+    return launch_dependent(layout_finish_kernel<true>, p.num_tiles, kFinishThreads,
+                            sizeof(int32_t) * E, stream, static_cast<const int32_t*>(tile_counts),
+                            p.num_tiles, E, N, p.tile, counts, offsets, slot);
 }
 
 }  // namespace ep

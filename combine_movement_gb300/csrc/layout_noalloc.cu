@@ -17,10 +17,11 @@
 // cudaGetSymbolAddress and caches it. That first call should therefore be
 // made before any stream capture.
 //
-// Sharing: every call uses the same array. Each call rewrites the words it
-// uses before reading them, so nothing has to start at zero, but calls that
-// overlap on the GPU (different streams, or different host threads) race on
-// the array and must be ordered by the caller.
+// Sharing: every call uses the same array. Each call rewrites the counts it
+// reads, and the single generation word it carries from call to call is
+// valid from any starting value, so nothing has to start at zero; but calls
+// that overlap on the GPU (different streams, or different host threads)
+// race on the array and must be ordered by the caller.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -80,7 +81,7 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(const int64_t* topk_idx, i
         if (st != EP_OK) return st;
     }
     const cudaError_t err =
-        ep::launch_layout(topk_idx, T * K, E, counts, offsets, slot, static_cast<int32_t*>(scratch),
-                          plan, status, static_cast<cudaStream_t>(stream));
+        ep::launch_layout(topk_idx, T * K, E, counts, offsets, slot, scratch, plan, status,
+                          static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }

@@ -166,6 +166,19 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
                  : "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel on the stream is still running; griddep_wait() blocks
+// until that kernel has completed and its memory is visible, so it must come
+// before the first global-memory access. griddep_launch_dependents() lets the
+// next such kernel begin launching now. Both are no-ops for ordinary launches.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Record the first device-side error (0 = none so far).
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
     if (status != nullptr) atomicCAS(status, 0, code);

@@ -53,6 +53,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_num_sms_in_effect.restype = i32
     lib.ep_layout_workspace_bytes.argtypes = [i64, i32, i32]
     lib.ep_layout_workspace_bytes.restype = sz
+    lib.ep_layout_launches.argtypes = [i64, i32, i32]
+    lib.ep_layout_launches.restype = i32
     lib.ep_get_dispatch_layout.argtypes = [p, i64, i32, i32, p, p, p, p, sz, p, p]
     lib.ep_get_dispatch_layout.restype = i32
     lib.ep_dispatch.argtypes = [p, i64, i64, i32, p, p, i64, p, p, p, p, p]
@@ -118,14 +120,8 @@ def ep_layout_workspace_bytes(T: int, K: int, E: int) -> int:
     return int(lib.ep_layout_workspace_bytes(T, K, E))
 
 
-def layout_launches(T: int, K: int, E: int) -> int:
-    """Kernel launches one ep_get_dispatch_layout call makes for these sizes:
-    one fused launch when no workspace is needed, else a tile and a finish
-    launch (three, with a separate scan, for very large tables)."""
-    nbytes = ep_layout_workspace_bytes(T, K, E)
-    if nbytes == 0:
-        return 1
-    return 2 if nbytes // 4 // E <= 512 else 3
+def ep_layout_launches(T: int, K: int, E: int) -> int:
+    return int(lib.ep_layout_launches(T, K, E))
 
 
 def ep_status_string(code: int) -> str:

@@ -107,13 +107,23 @@ EP_API int ep_num_sms_in_effect(void);
  * (0 when none; then `workspace` may be NULL). Depends on sizes only. */
 EP_API size_t ep_layout_workspace_bytes(int64_t T, int K, int E);
 
+/* Kernel launches one ep_get_dispatch_layout call makes for these sizes on a
+ * GPU where all of its tiles can be resident at once (1 for tables of up to
+ * 128 tiles; 2 or 3 above that), for accounting in measurements; -1 for
+ * invalid sizes. */
+EP_API int ep_layout_launches(int64_t T, int K, int E);
+
 /* Layout (per-expert histogram, exclusive prefix sums and per-(token,k)
  * destination slot).
  *   topk_idx   int64 [T][K]   routing table (DeepEP's topk_idx)
  *   counts     int32 [E]      out: rows per expert
  *   offsets    int32 [E+1]    out: first row of each expert; offsets[E] = R
  *   slot       int32 [T][K]   out: receive row of (t,k), -1 if skipped
- *   workspace  device scratch of ep_layout_workspace_bytes(T,K,E) bytes
+ *   workspace  device scratch of ep_layout_workspace_bytes(T,K,E) bytes,
+ *              16-byte aligned. It carries a small generation word from one
+ *              call to the next (the kernels' grid barriers use it); any
+ *              initial content is valid, so it never needs clearing. Calls
+ *              that share a workspace must not overlap on the GPU.
  *   status     int32 device word, nullable (device errors: BAD_EXPERT)
  * T == 0 is valid (counts and offsets are zeroed). */
 EP_API ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, int E,
@@ -165,7 +175,8 @@ EP_API ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv,
  *    capture.
  *  - Sharing: all calls share the array. Calls that overlap on the GPU (other
  *    streams or host threads) race on it; order them. Nothing in it needs to
- *    start at zero: each call rewrites what it reads. */
+ *    start at zero: each call rewrites the counts it reads, and the one word
+ *    it carries between calls is valid from any starting value. */
 #define EP_NOALLOC_SCRATCH_BYTES (1u << 20)
 EP_API ep_status_t ep_get_dispatch_layout_noalloc(const int64_t* topk_idx, int64_t T, int K, int E,
                                                   int32_t* counts, int32_t* offsets, int32_t* slot,

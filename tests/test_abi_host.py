@@ -67,9 +67,16 @@ def test_workspace_bytes(ep):
     assert ep.ep_layout_workspace_bytes(128, 8, 256) == 0          # one fused launch
     big = ep.ep_layout_workspace_bytes(4096, 8, 256)
     assert big > 0 and big % 4 == 0
-    assert big % (4 * 256) == 0 and big // (4 * 256) > 1             # E x tiles int32
+    assert big % 4 == 0 and big > 4 * 256 * 2                        # barrier words, totals, E x tiles
     assert ep.ep_layout_workspace_bytes(4096, 33, 256) == 0        # invalid -> 0
     assert ep.ep_layout_workspace_bytes(10, 2, 5000) == 0
+
+
+def test_layout_launch_counts(ep):
+    assert ep.ep_layout_launches(128, 8, 256) == 1       # one tile: fused block
+    assert ep.ep_layout_launches(4096, 8, 256) == 1      # few tiles: one cooperative launch
+    assert ep.ep_layout_launches(20000, 8, 4096) == 2    # many tiles: tile + finish launches
+    assert ep.ep_layout_launches(10, 33, 8) == -1
 
 
 def _raw(ep):

@@ -184,6 +184,8 @@ def _custom(T, H, E, K, seed=7, mask=0.0, routing="uniform"):
     (40, 64, 40, 32, 0.0),      # maximum K (generic combine path)
     (100, 128, 16, 12, 0.1),    # K above the specialised range, masked
     (9000, 64, 256, 1, 0.0),    # K = 1, multi-tile layout
+    (20000, 16, 4096, 8, 0.05), # more tiles than one launch holds: tile + finish kernels
+    (70000, 8, 4096, 8, 0.0),   # over 512 tiles: separate one-block scan
 ])
 def test_edge_shapes(ep, T, H, E, K, mask):
     inp = _custom(T, H, E, K, mask=mask)
