@@ -192,9 +192,17 @@ class Step:
     def combine(self, b: Buffers, stream=None):
         self.ep.ep_combine(self.expert_out, b.slot, b.w, b.y, b.status, stream)
 
+    def layout_dispatch(self, b: Buffers, stream=None):
+        self.ep.ep_layout_dispatch(b.idx, self.E, b.x, b.counts, b.offsets, b.slot, b.recv_x,
+                                   None, None, None, b.status, stream)
+
     def run(self, b: Buffers, stream=None):
         self.layout(b, stream)
         self.dispatch(b, stream)
+        self.combine(b, stream)
+
+    def run_fused(self, b: Buffers, stream=None):
+        self.layout_dispatch(b, stream)
         self.combine(b, stream)
 
     @property
@@ -253,6 +261,33 @@ def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch
     com = [ev[i][2].elapsed_time(ev[i][3]) for i in range(steps)]
     return {"total_ms": total_ms, "layout_ms": lay, "dispatch_ms": dis, "combine_ms": com,
             "clocks": sampler.summary() if sampler else None}
+
+
+def time_fused_steps(step: Step, steps: int, warmup: int, dist_on: bool,
+                     stream: torch.cuda.Stream) -> dict:
+    """The same step with layout and dispatch in one call (ep_layout_dispatch)."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step.run_fused(step.b, stream)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(dist_on)
+        start.record(stream)
+        for i in range(steps):
+            e = ev[i]
+            e[0].record(stream)
+            step.layout_dispatch(step.b, stream)
+            e[1].record(stream)
+            step.combine(step.b, stream)
+            e[2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist_on)
+    return {"total_ms": start.elapsed_time(end),
+            "layout_dispatch_ms": [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)],
+            "combine_ms": [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]}
 
 
 def time_e2e(step: Step, inp: W.Inputs, steps: int, warmup: int) -> dict:
@@ -370,6 +405,94 @@ def wl_desc(wl: W.Workload) -> str:
 
 
 # ---------------------------------------------------------------------------
+# per-kernel timing with a cold L2 (decode latency, SM-budget sweep)
+
+class _Flusher:
+    """Writes a buffer larger than L2 between timed calls."""
+
+    def __init__(self, dev):
+        self.buf = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def time_call(fn, reps: int, flush=None) -> float:
+    """Median microseconds of fn() on the current stream (CUDA events). The
+    GPU is kept busy (L2 flush, or a short spin) while the host enqueues the
+    call, so host launch overhead is not counted."""
+    ts = []
+    for i in range(reps + 3):
+        if flush is not None:
+            flush()
+        else:
+            torch.cuda._sleep(40000)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            ts.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(ts)
+
+
+def decode_latency(ep, dev, budgets=(16, 24, 0)) -> dict:
+    """Per-call latency of layout + dispatch + combine on the decode
+    workload (T=128, H=7168, E=256, top-8; 16.5 MB, L2-resident when warm)."""
+    wl = W.DECODE
+    step = Step(ep, W.make_inputs(wl), dev)
+    flush = _Flusher(dev)
+    ab = algorithmic_bytes(wl.T, wl.H, wl.K, wl.E, wl.T * wl.K)
+    out = {"workload": wl_desc(wl)}
+    for b in budgets:
+        ep.ep_set_num_sms(b)
+        warm = time_call(lambda: step.run(step.b), 200)
+        cold = time_call(lambda: step.run(step.b), 30, flush)
+        fwarm = time_call(lambda: step.run_fused(step.b), 200)
+        fcold = time_call(lambda: step.run_fused(step.b), 30, flush)
+        out[f"sms_{b or 'all'}"] = {
+            "warm_us": round(warm, 2), "cold_us": round(cold, 2),
+            "cold_gbs": round((ab["dispatch"] + ab["combine"]) / (cold * 1e-6) / 1e9, 1),
+            "fused_warm_us": round(fwarm, 2), "fused_cold_us": round(fcold, 2),
+        }
+    ep.ep_set_num_sms(0)
+    return out
+
+
+def run_sweep(ep, dev, budgets) -> None:
+    """SM-budget and size sweep: one JSON line per (T, H, budget) with each
+    kernel's median time (cold L2) and GB/s against the HBM peak."""
+    peak, _ = peak_hbm()
+    flush = _Flusher(dev)
+    sms_all = torch.cuda.get_device_properties(dev).multi_processor_count
+    for T in W.SWEEP_T:
+        for H in W.SWEEP_H:
+            wl = W.sweep(T, H)
+            step = Step(ep, W.make_inputs(wl), dev)
+            ab = algorithmic_bytes(T, H, wl.K, wl.E, T * wl.K)
+            for b in budgets:
+                ep.ep_set_num_sms(b)
+                lay = time_call(lambda: step.layout(step.b), 20, flush)
+                dis = time_call(lambda: step.dispatch(step.b), 20, flush)
+                com = time_call(lambda: step.combine(step.b), 20, flush)
+                gbs = (ab["dispatch"] + ab["combine"]) / ((dis + com) * 1e-6) / 1e9
+                print(json.dumps({
+                    "T": T, "H": H, "E": wl.E, "K": wl.K, "num_sms": b or sms_all,
+                    "layout_us": round(lay, 1), "dispatch_us": round(dis, 1),
+                    "combine_us": round(com, 1),
+                    "dispatch_gbs": round(ab["dispatch"] / (dis * 1e-6) / 1e9),
+                    "combine_gbs": round(ab["combine"] / (com * 1e-6) / 1e9),
+                    "dispatch_combine_gbs": round(gbs), "frac_of_peak": round(gbs / peak, 3),
+                    "tokens_per_s": round(T / ((lay + dis + com) * 1e-6)),
+                }), flush=True)
+            del step
+            torch.cuda.empty_cache()
+    ep.ep_set_num_sms(0)
+
+
+# ---------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser()
@@ -380,6 +503,8 @@ def main():
     ap.add_argument("--workload", default="deepseek-v3-prefill", choices=sorted(W.BY_NAME))
     ap.add_argument("--budget-sms", type=int, default=24, help="second SM budget to report")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: the T x H x SM-budget sweep, one JSON line each")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -404,6 +529,14 @@ def main():
     torch.cuda.set_device(dev)
     from combine_movement_gb300 import ep
 
+    if args.sweep:
+        if rank == 0:
+            run_sweep(ep, dev, budgets=(8, 16, 24, 48, 0))
+        if dist_on:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
     inp = W.make_inputs(wl)
     step = Step(ep, inp, dev)
     stream = torch.cuda.Stream(dev)
@@ -414,7 +547,12 @@ def main():
     ep.ep_set_num_sms(args.budget_sms)
     budget_run = time_steps(step, args.steps, args.warmup, dist_on, stream)
     ep.ep_set_num_sms(0)
+    fused_run = time_fused_steps(step, args.steps, args.warmup, dist_on, stream)
+    ep.ep_set_num_sms(args.budget_sms)
+    fused_budget = time_fused_steps(step, args.steps, args.warmup, dist_on, stream)
+    ep.ep_set_num_sms(0)
     e2e = time_e2e(step, inp, max(3, min(args.steps, 200)), 3)
+    decode = decode_latency(ep, dev) if rank == 0 else None
     st = ep.ep_get_status(step.b.status)
     if st != 0:
         raise SystemExit(f"device status {st}: {ep.ep_status_string(st)}")
@@ -437,6 +575,15 @@ def main():
             "dispatch_gbs": ab["dispatch"] / (d * 1e-3) / 1e9,
             "combine_gbs": ab["combine"] / (c * 1e-3) / 1e9,
         }
+
+    def summarize_fused(run: dict, nsms: int) -> dict:
+        ms = max_over_ranks(run["total_ms"] / args.steps, dist_on)
+        ld = statistics.mean(run["layout_dispatch_ms"])
+        c = statistics.mean(run["combine_ms"])
+        return {"num_sms": nsms, "ms_per_step": ms,
+                "tokens_per_s": world * step.T / (ms * 1e-3),
+                "layout_dispatch_us": 1e3 * ld, "combine_us": 1e3 * c,
+                "layout_dispatch_gbs": (ab["dispatch"] + ab["layout"]) / (ld * 1e-3) / 1e9}
 
     s_all = summarize(main_run, sms_all)
     s_bud = summarize(budget_run, min(args.budget_sms, sms_all))
@@ -471,6 +618,9 @@ def main():
             "hbm": {
                 "all_sms": s_all,
                 f"sms_{args.budget_sms}": s_bud,
+                "fused_all_sms": summarize_fused(fused_run, sms_all),
+                f"fused_sms_{args.budget_sms}": summarize_fused(fused_budget,
+                                                                min(args.budget_sms, sms_all)),
                 "peak_gbs": peak,
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_step": ab,
@@ -489,6 +639,7 @@ def main():
             "gpu_launches": step.launches_per_step * args.steps,
             "clocks": main_run["clocks"],
             "cpu_baseline": cpu,
+            "decode_latency": decode,
         }
         print(json.dumps(line), flush=True)
     if dist_on:

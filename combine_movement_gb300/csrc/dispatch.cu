@@ -28,6 +28,7 @@
 #include "../../include/ep.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "routing.cuh"
 
 namespace ep {
 namespace {
@@ -42,6 +43,12 @@ namespace {
 #ifndef EP_DISPATCH_PREFETCH
 #define EP_DISPATCH_PREFETCH 2
 #endif
+#ifndef EP_DISPATCH_STORE_FIRST
+#define EP_DISPATCH_STORE_FIRST 0
+#endif
+#ifndef EP_DISPATCH_LOAD_NORMAL
+#define EP_DISPATCH_LOAD_NORMAL 0
+#endif
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr int kDispatchWarps = EP_DISPATCH_WARPS;
@@ -52,8 +59,127 @@ __host__ __device__ constexpr uint32_t barrier_region(int stages, int warps) {
     return (8u * stages * warps + 127u) & ~127u;
 }
 
-template <int NS, int P>
-__global__ void __launch_bounds__(kDispatchWarps * 32, 1) dispatch_kernel(const DispatchArgs a) {
+// Layout prologue of the fused kernel (see dispatch_kernel). All threads of
+// the CTA take part; ends with a block barrier after which the slots of the
+// CTA's tokens are in global memory.
+__device__ __noinline__ void fused_layout(const DispatchArgs& a, const FusedLayoutArgs& f,
+                                          uint8_t* smem, int64_t units, int64_t nw_total) {
+    const int E = f.E;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int32_t* total = reinterpret_cast<int32_t*>(smem + f.hist_off);
+    int32_t* run = total + E;
+    const int64_t N = a.T * a.K;
+    // this CTA's tokens: the union of its warps' unit ranges
+    const int64_t cu0 = units * (static_cast<int64_t>(blockIdx.x) * nwarps) / nw_total;
+    const int64_t cu1 = units * (static_cast<int64_t>(blockIdx.x + 1) * nwarps) / nw_total;
+    const int64_t t0 = cu0 / a.n_chunks;
+    const int64_t t1 = cu1 > cu0 ? (cu1 - 1) / a.n_chunks + 1 : t0;
+    const int64_t i0 = t0 * a.K, i1 = t1 * a.K;
+
+    for (int e = threadIdx.x; e < E; e += blockDim.x) total[e] = run[e] = 0;
+    __syncthreads();
+    bool bad = false;
+    auto count = [&](int64_t i, int64_t v) {
+        const int e = expert_key(v, E);
+        if (e >= 0) {
+            atomicAdd(&total[e], 1);
+            if (i < i0) atomicAdd(&run[e], 1);
+        } else if (v != -1) {
+            bad = true;
+        }
+    };
+    // 16-byte loads (two ids each), 16 in flight per thread; an 8-byte-
+    // aligned first id and an odd last id are read on their own.
+    const int64_t head = (reinterpret_cast<uintptr_t>(f.idx) & 15u) ? 1 : 0;
+    const int64_t pairs = N > head ? (N - head) / 2 : 0;
+    const longlong2* pv = reinterpret_cast<const longlong2*>(f.idx + head);
+    constexpr int kBatch = 16;
+    for (int64_t b0 = threadIdx.x; b0 < pairs; b0 += static_cast<int64_t>(blockDim.x) * kBatch) {
+        longlong2 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int64_t q = b0 + static_cast<int64_t>(u) * blockDim.x;
+            v[u] = q < pairs ? __ldg(pv + q) : make_longlong2(-1, -1);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int64_t q = b0 + static_cast<int64_t>(u) * blockDim.x;
+            if (q < pairs) {
+                count(head + 2 * q, v[u].x);
+                count(head + 2 * q + 1, v[u].y);
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (head && N > 0) count(0, __ldg(f.idx));
+        const int64_t last = head + 2 * pairs;
+        if (last < N) count(last, __ldg(f.idx + last));
+    }
+    if (bad) set_status(a.status, EP_ERR_BAD_EXPERT);
+    __syncthreads();
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, per * static_cast<int>(threadIdx.x)), e1 = min(E, e0 + per);
+    int64_t local = 0;
+    for (int e = e0; e < e1; ++e) local += total[e];
+    int64_t all;
+    int64_t off = block_exclusive_scan(local, &all);
+    for (int e = e0; e < e1; ++e) {
+        if (blockIdx.x == 0) {
+            f.offsets[e] = static_cast<int32_t>(off);
+            f.counts[e] = total[e];
+        }
+        run[e] += static_cast<int32_t>(off);
+        off += total[e];
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) f.offsets[E] = static_cast<int32_t>(all);
+    __syncthreads();
+    if (warp == 0) {
+        // 8 rounds of ids are loaded together (one memory latency per 256
+        // entries), then ranked round by round in entry order.
+        const int kbits = key_bits_for(E);
+        constexpr int kRounds = 8;
+        for (int64_t b0 = i0; b0 < i1; b0 += 32 * kRounds) {
+            int key[kRounds];
+#pragma unroll
+            for (int r = 0; r < kRounds; ++r) {
+                const int64_t i = b0 + r * 32 + lane;
+                key[r] = i < i1 ? expert_key(__ldg(f.idx + i), E) : -1;
+            }
+#pragma unroll
+            for (int r = 0; r < kRounds; ++r) {
+                const int64_t i = b0 + r * 32 + lane;
+                if (b0 + r * 32 >= i1) break;
+                const uint32_t peers = peers_of(key[r], kbits);
+                if (i < i1)
+                    f.slot[i] = key[r] >= 0 ? run[key[r]] + __popc(peers & lanemask_lt()) : -1;
+                __syncwarp();
+                if (key[r] >= 0 && lane == __ffs(peers) - 1) run[key[r]] += __popc(peers);
+                __syncwarp();
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Plain (coherent) 32-bit load, for slots written earlier in the same kernel.
+__device__ __forceinline__ int32_t ld_plain_s32(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// FUSED: layout computed by every CTA for its own tokens before its ring
+// (ep_layout_dispatch). Each CTA reads the whole routing table once (it is
+// small next to the rows), keeping in shared memory each expert's total and
+// the number of entries before the CTA's first token; a scan across experts
+// gives each expert's first row; warp 0 then ranks the CTA's own entries in
+// entry order (per-bit ballot peer groups) and writes their slots. No CTA
+// waits on another and no workspace is needed. Block 0 writes counts and
+// offsets; a token split between two CTAs gets the same slots from both.
+template <int NS, int P, bool FUSED>
+__global__ void __launch_bounds__(kDispatchWarps * 32, 1)
+    dispatch_kernel(const DispatchArgs a, const FusedLayoutArgs f) {
     static_assert(P >= 1 && P < NS, "need 1 <= P < NS");
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -77,12 +203,23 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1) dispatch_kernel(const 
     const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
+    if (FUSED) fused_layout(a, f, smem, units, nw_total);
     const int64_t u0 = units * gw / nw_total;
     const int64_t n = units * (gw + 1) / nw_total - u0;
     if (n <= 0) return;
 
-    const uint64_t pol_load = policy_evict_first();
+    // L2 policies: x is read once (evict first); the receive rows are
+    // written once and next read by the experts (normal).
+#if EP_DISPATCH_STORE_FIRST
+    const uint64_t pol_store = policy_evict_first();
+#else
     const uint64_t pol_store = policy_evict_normal();
+#endif
+#if EP_DISPATCH_LOAD_NORMAL
+    const uint64_t pol_load = policy_evict_normal();
+#else
+    const uint64_t pol_load = policy_evict_first();
+#endif
 
     // Bulk-load local unit j (token, chunk) into its ring stage.
     auto issue_load = [&](int64_t j) {
@@ -101,7 +238,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1) dispatch_kernel(const 
     // Lanes k < K hold slot[t][k] (and topk_w[t][k]) of the current token and
     // of the next one, loaded a token ahead.
     auto load_slot = [&](int64_t t) -> int32_t {
-        return (t < a.T && lane < a.K) ? __ldg(a.slot + t * a.K + lane) : -1;
+        if (t >= a.T || lane >= a.K) return -1;
+        return FUSED ? ld_plain_s32(a.slot + t * a.K + lane) : __ldg(a.slot + t * a.K + lane);
     };
     auto load_w = [&](int64_t t) -> float {
         return (a.topk_w != nullptr && t < a.T && lane < a.K) ? __ldg(a.topk_w + t * a.K + lane)
@@ -249,7 +387,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, int smem_optin,
     const size_t smem = static_cast<size_t>(barrier_region(kStages, kDispatchWarps)) +
                         static_cast<size_t>(kDispatchWarps) * kStages * a.stage_bytes;
     const size_t request = smem < kExclusiveSmem ? kExclusiveSmem : smem;
-    auto kern = dispatch_kernel<kStages, kPrefetch>;
+    auto kern = dispatch_kernel<kStages, kPrefetch, false>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(request));
@@ -258,15 +396,34 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, int smem_optin,
     int64_t ctas_needed = (units + kDispatchWarps - 1) / kDispatchWarps;
     const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
     if (grid <= 0) return cudaSuccess;
-    return launch_dependent(kern, grid, kDispatchWarps * 32, request, stream, a);
+    return launch_dependent(kern, grid, kDispatchWarps * 32, request, stream, a, FusedLayoutArgs{});
 }
 
-// Stage size the host plans rows with: the per-warp slice split into the
-// ring's stages, rounded down to 16 bytes.
-uint32_t dispatch_stage_capacity(int smem_optin) {
-    const size_t per_warp =
-        (static_cast<size_t>(smem_optin) - barrier_region(kStages, kDispatchWarps)) / kDispatchWarps;
+// Stage size the host plans rows with: the per-warp slice (what is left of
+// the opt-in limit after `reserve` bytes) split into the ring's stages,
+// rounded down to 16 bytes.
+uint32_t dispatch_stage_capacity(int smem_optin, size_t reserve) {
+    const size_t avail = static_cast<size_t>(smem_optin) - barrier_region(kStages, kDispatchWarps);
+    if (avail <= reserve) return 0;
+    const size_t per_warp = (avail - reserve) / kDispatchWarps;
     return static_cast<uint32_t>((per_warp / kStages) & ~static_cast<size_t>(15));
+}
+
+cudaError_t launch_layout_dispatch(const DispatchArgs& a, FusedLayoutArgs f, int num_sms,
+                                   cudaStream_t stream) {
+    const size_t ring = static_cast<size_t>(barrier_region(kStages, kDispatchWarps)) +
+                        static_cast<size_t>(kDispatchWarps) * kStages * a.stage_bytes;
+    f.hist_off = static_cast<uint32_t>(ring);
+    size_t smem = ring + 2 * sizeof(int32_t) * static_cast<size_t>(f.E);
+    if (smem < kExclusiveSmem) smem = kExclusiveSmem;
+    auto kern = dispatch_kernel<kStages, kPrefetch, true>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
+    const int64_t ctas_needed = (units + kDispatchWarps - 1) / kDispatchWarps;
+    const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
+    return launch_dependent(kern, grid > 0 ? grid : 1, kDispatchWarps * 32, smem, stream, a, f);
 }
 
 }  // namespace ep

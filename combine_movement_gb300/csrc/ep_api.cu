@@ -78,6 +78,51 @@ bool use_combine_tma(int K, int num_sms) {
     return false;
 }
 
+// Host checks shared by ep_dispatch and ep_layout_dispatch.
+ep_status_t check_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const int32_t* slot,
+                           const float* topk_w, int64_t num_recv, const uint16_t* recv_x,
+                           const float* recv_w, const int32_t* recv_src, const int32_t* status) {
+    if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || num_recv < 0)
+        return EP_ERR_INVALID;
+    if (T * static_cast<int64_t>(K) >= (int64_t{1} << 31) || num_recv >= (int64_t{1} << 31) ||
+        H * 2 > 0x7FFFFFF0)
+        return EP_ERR_UNSUPPORTED;
+    if (T == 0) return EP_OK;
+    if (x == nullptr || slot == nullptr || (num_recv > 0 && recv_x == nullptr)) return EP_ERR_INVALID;
+    if (recv_w != nullptr && topk_w == nullptr) return EP_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(slot, 4) || !aligned(topk_w, 4) ||
+        !aligned(recv_w, 4) || !aligned(recv_src, 4) || !aligned(status, 4))
+        return EP_ERR_INVALID;
+    return EP_OK;
+}
+
+// Fills the kernel arguments: rows cut into equal 16-byte-multiple chunks
+// that each fit one ring stage (after `reserve` bytes of other shared data).
+ep_status_t plan_dispatch(ep::DispatchArgs* a, const uint16_t* x, int64_t T, int64_t H, int K,
+                          const int32_t* slot, const float* topk_w, int64_t num_recv,
+                          uint16_t* recv_x, float* recv_w, int32_t* recv_src, int32_t* status,
+                          int smem_optin, size_t reserve) {
+    a->x = reinterpret_cast<const uint8_t*>(x);
+    a->T = T;
+    a->row_bytes = static_cast<uint32_t>(H * 2);
+    a->K = K;
+    a->slot = slot;
+    a->topk_w = topk_w;
+    a->num_recv = num_recv;
+    a->recv_x = reinterpret_cast<uint8_t*>(recv_x);
+    a->recv_w = recv_w;
+    a->recv_src = recv_src;
+    a->status = status;
+    const uint32_t cap = ep::dispatch_stage_capacity(smem_optin, reserve);
+    if (cap < 16) return EP_ERR_UNSUPPORTED;
+    const uint32_t n_chunks = (a->row_bytes + cap - 1) / cap;
+    const uint32_t per = (a->row_bytes + n_chunks - 1) / n_chunks;
+    a->chunk_bytes = (per + 15u) & ~15u;
+    a->n_chunks = (a->row_bytes + a->chunk_bytes - 1) / a->chunk_bytes;
+    a->stage_bytes = a->chunk_bytes;
+    return EP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -132,42 +177,46 @@ ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, in
 ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const int32_t* slot,
                         const float* topk_w, int64_t num_recv, uint16_t* recv_x, float* recv_w,
                         int32_t* recv_src, int32_t* status, void* stream) {
-    if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || num_recv < 0)
-        return EP_ERR_INVALID;
-    if (T * static_cast<int64_t>(K) >= (int64_t{1} << 31) || num_recv >= (int64_t{1} << 31) ||
-        H * 2 > 0x7FFFFFF0)
-        return EP_ERR_UNSUPPORTED;
-    if (T == 0) return EP_OK;
-    if (x == nullptr || slot == nullptr || (num_recv > 0 && recv_x == nullptr)) return EP_ERR_INVALID;
-    if (recv_w != nullptr && topk_w == nullptr) return EP_ERR_INVALID;
-    if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(slot, 4) || !aligned(topk_w, 4) ||
-        !aligned(recv_w, 4) || !aligned(recv_src, 4) || !aligned(status, 4))
-        return EP_ERR_INVALID;
+    ep_status_t st = check_dispatch(x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src,
+                                    status);
+    if (st != EP_OK || T == 0) return st;
     int sm_count = 0, smem_optin = 0;
     if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
-
     ep::DispatchArgs a{};
-    a.x = reinterpret_cast<const uint8_t*>(x);
-    a.T = T;
-    a.row_bytes = static_cast<uint32_t>(H * 2);
-    a.K = K;
-    a.slot = slot;
-    a.topk_w = topk_w;
-    a.num_recv = num_recv;
-    a.recv_x = reinterpret_cast<uint8_t*>(recv_x);
-    a.recv_w = recv_w;
-    a.recv_src = recv_src;
-    a.status = status;
-    // Equal 16-byte-multiple chunks, each fitting one ring stage.
-    const uint32_t cap = ep::dispatch_stage_capacity(smem_optin);
-    if (cap < 16) return EP_ERR_UNSUPPORTED;
-    const uint32_t n_chunks = (a.row_bytes + cap - 1) / cap;
-    const uint32_t per = (a.row_bytes + n_chunks - 1) / n_chunks;
-    a.chunk_bytes = (per + 15u) & ~15u;
-    a.n_chunks = (a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes;
-    a.stage_bytes = a.chunk_bytes;
+    st = plan_dispatch(&a, x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src, status,
+                       smem_optin, 0);
+    if (st != EP_OK) return st;
     return from_cuda(ep::launch_dispatch(a, sms_in_effect(sm_count), smem_optin,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64_t T, int64_t H,
+                               int K, int E, const float* topk_w, int64_t num_recv, int32_t* counts,
+                               int32_t* offsets, int32_t* slot, uint16_t* recv_x, float* recv_w,
+                               int32_t* recv_src, int32_t* status, void* stream) {
+    if (E < 1) return EP_ERR_INVALID;
+    if (E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
+    if (counts == nullptr || offsets == nullptr || !aligned(counts, 4) || !aligned(offsets, 4))
+        return EP_ERR_INVALID;
+    if (T > 0 && (topk_idx == nullptr || !aligned(topk_idx, 8))) return EP_ERR_INVALID;
+    ep_status_t st = check_dispatch(x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src,
+                                    status);
+    if (st != EP_OK) return st;
+    int sm_count = 0, smem_optin = 0;
+    if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
+    ep::DispatchArgs a{};
+    const size_t hist = 2 * sizeof(int32_t) * static_cast<size_t>(E);
+    st = plan_dispatch(&a, x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src, status,
+                       smem_optin, hist);
+    if (st != EP_OK) return st;
+    ep::FusedLayoutArgs f{};
+    f.idx = topk_idx;
+    f.E = E;
+    f.counts = counts;
+    f.offsets = offsets;
+    f.slot = slot;
+    return from_cuda(ep::launch_layout_dispatch(a, f, sms_in_effect(sm_count),
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv, const int32_t* slot,

@@ -50,12 +50,28 @@ struct DispatchArgs {
     uint32_t stage_bytes;  // shared-memory bytes per ring stage (>= chunk_bytes)
 };
 
+// Routing inputs and layout outputs of the fused layout + dispatch kernel.
+struct FusedLayoutArgs {
+    const int64_t* idx;
+    int E;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* slot;      // the same array as DispatchArgs::slot, written by the kernel
+    uint32_t hist_off;  // shared-memory byte offset of its 2*E histogram words
+};
+
 cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, int smem_optin,
                             cudaStream_t stream);
 
+// Layout and dispatch in one launch (every CTA computes the layout of its
+// own tokens). a.slot must equal f.slot.
+cudaError_t launch_layout_dispatch(const DispatchArgs& a, FusedLayoutArgs f, int num_sms,
+                                   cudaStream_t stream);
+
 // Largest ring stage (bytes, multiple of 16) dispatch can use on a device
-// whose per-block shared-memory opt-in limit is `smem_optin`.
-uint32_t dispatch_stage_capacity(int smem_optin);
+// whose per-block shared-memory opt-in limit is `smem_optin`, after
+// reserving `reserve` bytes for other shared data.
+uint32_t dispatch_stage_capacity(int smem_optin, size_t reserve);
 
 // ---- combine --------------------------------------------------------------
 

@@ -33,13 +33,14 @@
 #include "../../include/ep.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "routing.cuh"
 
 namespace ep {
 namespace {
 
-constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr size_t kRunSmemBudget = 64 * 1024;  // per-warp expert counters of the tile kernel
 constexpr int kMaxRounds = 8;                 // 32-entry rounds per warp per tile, at most
+constexpr int kFusedRounds = 1;               // one block alone up to this many rounds
 constexpr int kTargetTiles = 128;             // tiles to aim for before rounds grow
 constexpr int kMaxRedundantTiles = 512;       // above this, one block scans for everyone
 constexpr int kCoopMaxTiles = 128;            // tables of at most this many tiles: one launch
@@ -48,68 +49,6 @@ constexpr int kFinishThreads = 512;
 constexpr int kExpertBits = 12;               // packed entry: (rank << 12) | expert, E <= 4096
 constexpr int32_t kExpertMask = (1 << kExpertBits) - 1;
 static_assert((1 << kExpertBits) >= EP_MAX_EXPERTS, "expert id must fit the packed entry");
-
-__device__ __forceinline__ uint32_t lanemask_lt() {
-    uint32_t m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
-
-// Expert id of a table cell, or -1 when the cell is masked (-1) or invalid.
-__device__ __forceinline__ int expert_key(int64_t v, int E) {
-    return (v >= 0 && v < E) ? static_cast<int>(v) : -1;
-}
-
-// Exclusive scan of one value per thread across the block (blockDim.x a
-// multiple of 32, at most 1024). Returns the exclusive prefix; *total gets
-// the block sum. Contains __syncthreads(); every thread must call it.
-__device__ int64_t block_exclusive_scan(int64_t v, int64_t* total) {
-    __shared__ int64_t warp_base[32];
-    __shared__ int64_t block_total;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    int64_t incl = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int64_t o = __shfl_up_sync(kFullMask, incl, d);
-        if (lane >= d) incl += o;
-    }
-    if (lane == 31) warp_base[warp] = incl;  // warp sum
-    __syncthreads();
-    if (warp == 0) {
-        const int64_t s = lane < nwarps ? warp_base[lane] : 0;
-        int64_t si = s;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int64_t o = __shfl_up_sync(kFullMask, si, d);
-            if (lane >= d) si += o;
-        }
-        if (lane < nwarps) warp_base[lane] = si - s;  // exclusive warp base
-        if (lane == 31) block_total = si;
-    }
-    __syncthreads();
-    const int64_t out = warp_base[warp] + incl - v;
-    *total = block_total;
-    __syncthreads();  // the shared words may be reused by a later call
-    return out;
-}
-
-// Lanes of the warp whose key equals this lane's key (all invalid lanes,
-// key -1, form one group). Built from one ballot per key bit: a handful of
-// single-cycle votes instead of a warp match.
-__device__ __forceinline__ uint32_t peers_of(int key, int key_bits) {
-    const uint32_t valid = __ballot_sync(kFullMask, key >= 0);
-    uint32_t m = key >= 0 ? valid : ~valid;
-    for (int b = 0; b < key_bits; ++b) {
-        const bool bit = (key >> b) & 1;
-        const uint32_t ones = __ballot_sync(kFullMask, bit);
-        m &= bit ? ones : ~ones;
-    }
-    return m;
-}
-
-// Bits needed for expert ids 0..E-1.
-__device__ __forceinline__ int key_bits_for(int E) { return E > 1 ? 32 - __clz(E - 1) : 0; }
 
 // Exclusive scan across the block's warps of the per-warp counts
 // run[w][e], one expert per thread (in place); writes the tile total of
@@ -513,7 +452,7 @@ LayoutPlan plan_layout(int64_t N, int E) {
     warps = warps < 1 ? 1 : (warps > 32 ? 32 : warps);
     p.warps = warps;
     const int64_t per_round = 32LL * warps;  // entries per round of the whole block
-    if (N <= per_round * kMaxRounds) {
+    if (N <= per_round * kFusedRounds) {
         p.num_tiles = 1;
         p.rounds = static_cast<int>((N + per_round - 1) / per_round);
         if (p.rounds < 1) p.rounds = 1;
@@ -522,7 +461,7 @@ LayoutPlan plan_layout(int64_t N, int E) {
         p.rounds = static_cast<int>(r < 1 ? 1 : (r > kMaxRounds ? kMaxRounds : r));
     }
     p.tile = per_round * p.rounds;
-    if (N > per_round * kMaxRounds) p.num_tiles = static_cast<int>((N + p.tile - 1) / p.tile);
+    if (N > per_round * kFusedRounds) p.num_tiles = static_cast<int>((N + p.tile - 1) / p.tile);
     p.smem = sizeof(int32_t) * static_cast<size_t>(E) * warps;
     p.coop = p.num_tiles > 1 && p.num_tiles <= kCoopMaxTiles;
     if (p.num_tiles > 1) {

@@ -59,6 +59,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_get_dispatch_layout.restype = i32
     lib.ep_dispatch.argtypes = [p, i64, i64, i32, p, p, i64, p, p, p, p, p]
     lib.ep_dispatch.restype = i32
+    lib.ep_layout_dispatch.argtypes = [p, p, i64, i64, i32, i32, p, i64, p, p, p, p, p, p, p, p]
+    lib.ep_layout_dispatch.restype = i32
     lib.ep_combine.argtypes = [p, i64, p, p, i64, i64, i32, p, p, p]
     lib.ep_combine.restype = i32
     lib.ep_get_dispatch_layout_noalloc.argtypes = [p, i64, i32, i32, p, p, p, p, p]
@@ -172,6 +174,24 @@ def ep_dispatch(x: torch.Tensor, slot: torch.Tensor, recv_x: torch.Tensor,
         _ptr(recv_src, torch.int32, "recv_src"), _ptr(status, torch.int32, "status"),
         _stream(stream))
     _check(code, "ep_dispatch")
+
+
+def ep_layout_dispatch(topk_idx: torch.Tensor, num_experts: int, x: torch.Tensor,
+                       counts: torch.Tensor, offsets: torch.Tensor, slot: torch.Tensor,
+                       recv_x: torch.Tensor, topk_w: Optional[torch.Tensor] = None,
+                       recv_w: Optional[torch.Tensor] = None,
+                       recv_src: Optional[torch.Tensor] = None,
+                       status: Optional[torch.Tensor] = None, stream=None) -> None:
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    code = lib.ep_layout_dispatch(
+        _ptr(topk_idx, torch.int64, "topk_idx"), _ptr(x, torch.bfloat16, "x"), T, H, K,
+        int(num_experts), _ptr(topk_w, torch.float32, "topk_w"), recv_x.shape[0],
+        _ptr(counts, torch.int32, "counts"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(slot, torch.int32, "slot"), _ptr(recv_x, torch.bfloat16, "recv_x"),
+        _ptr(recv_w, torch.float32, "recv_w"), _ptr(recv_src, torch.int32, "recv_src"),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(code, "ep_layout_dispatch")
 
 
 def ep_combine(expert_out: torch.Tensor, slot: torch.Tensor, topk_w: torch.Tensor,

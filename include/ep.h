@@ -147,6 +147,21 @@ EP_API ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K,
                         uint16_t* recv_x, float* recv_w, int32_t* recv_src,
                         int32_t* status, void* stream);
 
+/* Layout and dispatch in one launch: the results of ep_get_dispatch_layout
+ * (counts, offsets, slot) and of ep_dispatch (recv_x, recv_w, recv_src),
+ * identical to calling the two in turn, with no workspace. Every CTA reads
+ * the whole routing table and histograms it in shared memory to lay out its
+ * own tokens, so its cost grows with T*K per CTA: it is the call for
+ * decode-size batches (on GB300, T=128 top-8: 24 us per layout + dispatch +
+ * combine instead of 27 us), while prefill-size tables are as fast or faster
+ * with the two separate calls. Arguments as in those two calls; T == 0
+ * still writes zero counts and offsets. */
+EP_API ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64_t T,
+                                      int64_t H, int K, int E, const float* topk_w,
+                                      int64_t num_recv, int32_t* counts, int32_t* offsets,
+                                      int32_t* slot, uint16_t* recv_x, float* recv_w,
+                                      int32_t* recv_src, int32_t* status, void* stream);
+
 /* Combine: weighted gather of the K expert rows of every token back into
  * token order (arithmetic in the header comment above).
  *   expert_out bf16 [num_recv][H]  rows in receive order

@@ -109,3 +109,10 @@ def test_host_argument_checks(ep):
     assert lib.ep_get_dispatch_layout(A, 4096, 8, 256, A, A, A, None, 0, None, None) == ep.EP_ERR_WORKSPACE
     assert lib.ep_get_dispatch_layout(A, 4096, 8, 256, A, A, A, A, 64, None, None) == ep.EP_ERR_WORKSPACE
     assert lib.ep_get_status(None, None) == ep.EP_ERR_INVALID
+    # fused layout + dispatch
+    ld = lib.ep_layout_dispatch
+    assert ld(A, A, 4, 16, 2, 0, None, 8, A, A, A, A, None, None, None, None) == ep.EP_ERR_INVALID
+    assert ld(A, A, 4, 16, 2, 5000, None, 8, A, A, A, A, None, None, None, None) == ep.EP_ERR_UNSUPPORTED
+    assert ld(A, A, 4, 12, 2, 8, None, 8, A, A, A, A, None, None, None, None) == ep.EP_ERR_INVALID
+    assert ld(A + 4, A, 4, 16, 2, 8, None, 8, A, A, A, A, None, None, None, None) == ep.EP_ERR_INVALID
+    assert ld(A, A, 4, 16, 2, 8, None, 8, None, A, A, A, None, None, None, None) == ep.EP_ERR_INVALID

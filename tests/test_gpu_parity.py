@@ -87,7 +87,7 @@ def oracle_path(inp: W.Inputs, num_recv: int, expert_scale: float) -> Ref:
 
 
 def gpu_path(ep, inp: W.Inputs, num_recv: int, expert_out: np.ndarray, num_sms: int = 0,
-             stream=None):
+             stream=None, fused: bool = False):
     dev = torch.device("cuda:0")
     E = inp.wl.E
     ep.ep_set_num_sms(num_sms)
@@ -107,8 +107,12 @@ def gpu_path(ep, inp: W.Inputs, num_recv: int, expert_out: np.ndarray, num_sms: 
     recv_src = torch.full((num_recv,), -1, dtype=torch.int32, device=dev)
     y = torch.full((T, inp.wl.H), 3.0, dtype=torch.bfloat16, device=dev)
     eo = from_bits(expert_out).to(dev)
-    ep.ep_get_dispatch_layout(idx, E, counts, offsets, slot, ws, status, stream)
-    ep.ep_dispatch(x, slot, recv_x, w, recv_w, recv_src, status, stream)
+    if fused:
+        ep.ep_layout_dispatch(idx, E, x, counts, offsets, slot, recv_x, w, recv_w, recv_src,
+                              status, stream)
+    else:
+        ep.ep_get_dispatch_layout(idx, E, counts, offsets, slot, ws, status, stream)
+        ep.ep_dispatch(x, slot, recv_x, w, recv_w, recv_src, status, stream)
     ep.ep_combine(eo, slot, w, y, status, stream)
     st = ep.ep_get_status(status, stream)
     torch.cuda.synchronize()
@@ -283,3 +287,48 @@ def test_side_stream_and_repeat_determinism(ep):
     assert_parity(a, ref)
     for k in a:
         assert np.array_equal(a[k], b[k], equal_nan=True)
+
+
+# ---- ep_layout_dispatch: layout and dispatch in one launch -----------------
+
+@pytest.mark.parametrize("name,budgets", [
+    ("tiny", (0, 3)),
+    ("decode", (0, 16, 24)),
+    ("skewed", (0, 24)),
+    ("deepseek", (0, 8, 24)),
+])
+def test_fused_layout_dispatch_workloads(ep, name, budgets):
+    inp, ref = _case(name)
+    for b in budgets:
+        got = gpu_path(ep, inp, inp.wl.T * inp.wl.K, ref.expert_out, num_sms=b, fused=True)
+        assert_parity(got, ref)
+
+
+@pytest.mark.parametrize("T,H,E,K,mask", [
+    (0, 64, 8, 2, 0.0),
+    (1, 8, 1, 1, 0.0),
+    (3, 24, 2, 2, 0.0),
+    (257, 16384, 16, 4, 0.0),
+    (500, 1024, 128, 6, 0.3),
+    (64, 256, 4096, 8, 0.0),
+    (40, 64, 40, 32, 0.0),
+    (2000, 64, 256, 1, 0.1),
+])
+def test_fused_layout_dispatch_edges(ep, T, H, E, K, mask):
+    inp = _custom(T, H, E, K, mask=mask)
+    R_valid = int((inp.topk_idx >= 0).sum())
+    ref = oracle_path(inp, R_valid + 3, 1.0)
+    for b in (0, 5):
+        assert_parity(gpu_path(ep, inp, R_valid + 3, ref.expert_out, num_sms=b, fused=True), ref)
+
+
+def test_fused_layout_dispatch_bad_ids(ep):
+    inp = _custom(300, 64, 32, 4)
+    idx = inp.topk_idx.clone()
+    idx[5, 1] = 99
+    idx[200, 0] = -4
+    inp = dataclasses.replace(inp, topk_idx=idx.contiguous())
+    ref = oracle_path(inp, 300 * 4, 1.0)
+    got = gpu_path(ep, inp, 300 * 4, ref.expert_out, fused=True)
+    assert got["status"] == ep.EP_ERR_BAD_EXPERT
+    assert_parity(got, ref)
