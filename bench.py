@@ -505,6 +505,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: the T x H x SM-budget sweep, one JSON line each")
+    ap.add_argument("--only-main", action="store_true",
+                    help="for profiling: only the all-SM timed loop (no 24-SM, fused, e2e or "
+                         "decode passes)")
+    ap.add_argument("--ncu-budgets", action="store_true",
+                    help="for profiling: one layout+dispatch+combine step at each SM budget "
+                         "(16, 24, 48, all), after one warm-up step")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -529,6 +535,16 @@ def main():
     torch.cuda.set_device(dev)
     from combine_movement_gb300 import ep
 
+    if args.ncu_budgets:
+        step = Step(ep, W.make_inputs(wl), dev)
+        for b in (0, 16, 24, 48, 0):
+            ep.ep_set_num_sms(b)
+            step.run(step.b)
+            torch.cuda.synchronize(dev)
+        ep.ep_set_num_sms(0)
+        print(json.dumps({"ncu_budgets": [16, 24, 48, "all"], "status": ep.ep_get_status(step.b.status)}))
+        return
+
     if args.sweep:
         if rank == 0:
             run_sweep(ep, dev, budgets=(8, 16, 24, 48, 0))
@@ -544,6 +560,12 @@ def main():
 
     ep.ep_set_num_sms(0)
     main_run = time_steps(step, args.steps, args.warmup, dist_on, stream, sampler_index=local)
+    if args.only_main:
+        ms = max_over_ranks(main_run["total_ms"] / args.steps, dist_on)
+        if rank == 0:
+            print(json.dumps({"only_main": True, "ms_per_step": ms,
+                              "tokens_per_s": world * step.T / (ms * 1e-3)}), flush=True)
+        return
     ep.ep_set_num_sms(args.budget_sms)
     budget_run = time_steps(step, args.steps, args.warmup, dist_on, stream)
     ep.ep_set_num_sms(0)
