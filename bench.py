@@ -493,6 +493,111 @@ def run_sweep(ep, dev, budgets) -> None:
 
 
 # ---------------------------------------------------------------------------
+# bandwidth ceilings of this GPU (for reading the roofline fractions)
+
+_CEILING_SRC = r"""
+#include <cuda_runtime.h>
+#include <cstdint>
+__global__ void k_write(uint4* p, size_t n16) {
+    const uint4 v = make_uint4(1, 2, 3, 4);
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
+         i += (size_t)gridDim.x * blockDim.x) p[i] = v;
+}
+__global__ void k_read(const uint4* p, size_t n16, uint32_t* sink) {
+    uint32_t acc = 0;
+    size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x, s = (size_t)gridDim.x * blockDim.x;
+    for (; i + 3 * s < n16; i += 4 * s) {
+        uint4 a = __ldcs(p + i), b = __ldcs(p + i + s), c = __ldcs(p + i + 2 * s), d = __ldcs(p + i + 3 * s);
+        acc ^= a.x ^ b.y ^ c.z ^ d.w;
+    }
+    for (; i < n16; i += s) acc ^= __ldcs(p + i).x;
+    if (acc == 0x12345678u) *sink = acc;
+}
+__global__ void k_copy(const uint4* a, uint4* b, size_t n16) {
+    size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x, s = (size_t)gridDim.x * blockDim.x;
+    for (; i + s < n16; i += 2 * s) { uint4 x = __ldcs(a + i), y = __ldcs(a + i + s); b[i] = x; b[i + s] = y; }
+    for (; i < n16; i += s) b[i] = __ldcs(a + i);
+}
+__global__ void k_bulk_write(uint8_t* dst, size_t nbytes) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
+    uint8_t* my = sm + warp * 8192;
+    for (int i = lane; i < 8192 / 4; i += 32) reinterpret_cast<uint32_t*>(my)[i] = i;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        size_t chunks = nbytes / 8192, gw = blockIdx.x * (size_t)nw + warp, W = (size_t)gridDim.x * nw;
+        uint32_t src = (uint32_t)__cvta_generic_to_shared(my);
+        int n = 0;
+        for (size_t c = gw; c < chunks; c += W) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                         :: "l"(dst + c * 8192), "r"(src), "r"(8192) : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            if (++n >= 8) { asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory"); n = 4; }
+        }
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
+}
+extern "C" {
+int bw_write(void* p, size_t n, int grid, int block) { k_write<<<grid, block>>>((uint4*)p, n / 16); return cudaGetLastError(); }
+int bw_read(void* p, size_t n, void* sink, int grid, int block) { k_read<<<grid, block>>>((const uint4*)p, n / 16, (uint32_t*)sink); return cudaGetLastError(); }
+int bw_copy(void* a, void* b, size_t n, int grid, int block) { k_copy<<<grid, block>>>((const uint4*)a, (uint4*)b, n / 16); return cudaGetLastError(); }
+int bw_bulk_write(void* p, size_t n, int grid, int warps) {
+    cudaFuncSetAttribute(k_bulk_write, cudaFuncAttributeMaxDynamicSharedMemorySize, warps * 8192);
+    k_bulk_write<<<grid, warps * 32, warps * 8192>>>((uint8_t*)p, n); return cudaGetLastError(); }
+}
+"""
+
+
+def measure_ceilings(dev) -> dict:
+    """Write-only, read-only and copy bandwidth of plain streaming kernels
+    (16-byte vectors; 8 KB bulk stores), all SMs and 24 SMs, plus pinned
+    host<->device copy rates. Built from the source above with nvcc."""
+    import ctypes
+    import tempfile
+    tmp = tempfile.mkdtemp(prefix="ep_ceilings_")
+    src, so = os.path.join(tmp, "bw.cu"), os.path.join(tmp, "libbw.so")
+    with open(src, "w") as f:
+        f.write(_CEILING_SRC)
+    subprocess.run(["nvcc", "-O3", "-shared", "-Xcompiler", "-fPIC",
+                    "-gencode=arch=compute_103a,code=sm_103a", "-o", so, src], check=True)
+    L = ctypes.CDLL(so)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    n = 1 << 30
+    a = torch.ones(n, dtype=torch.uint8, device=dev)
+    b = torch.empty(n, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def best(fn, nbytes):
+        ts = []
+        for i in range(12):
+            s_ = torch.cuda.Event(enable_timing=True)
+            e_ = torch.cuda.Event(enable_timing=True)
+            s_.record()
+            assert fn() == 0
+            e_.record()
+            torch.cuda.synchronize()
+            if i >= 2:
+                ts.append(s_.elapsed_time(e_))
+        return round(nbytes / (min(ts) * 1e-3) / 1e9)
+
+    r = {}
+    for tag, g, blk in (("all_sms", sms * 8, 512), ("sms_24", 24, 1024)):
+        r[f"write_{tag}"] = best(lambda: L.bw_write(vp(a.data_ptr()), sz(n), g, blk), n)
+        r[f"read_{tag}"] = best(lambda: L.bw_read(vp(a.data_ptr()), sz(n), vp(sink.data_ptr()), g, blk), n)
+        r[f"copy_{tag}"] = best(lambda: L.bw_copy(vp(a.data_ptr()), vp(b.data_ptr()), sz(n), g, blk), 2 * n)
+    r["bulk_write_all_sms"] = best(lambda: L.bw_bulk_write(vp(a.data_ptr()), sz(n), sms, 8), n)
+    r["bulk_write_sms_24"] = best(lambda: L.bw_bulk_write(vp(a.data_ptr()), sz(n), 24, 24), n)
+    m = 59 * 1024 * 1024
+    h = torch.ones(m, dtype=torch.uint8).pin_memory()
+    d = torch.empty(m, dtype=torch.uint8, device=dev)
+    r["h2d_gbs"] = best(lambda: (d.copy_(h, non_blocking=True), 0)[1], m)
+    r["d2h_gbs"] = best(lambda: (h.copy_(d, non_blocking=True), 0)[1], m)
+    return r
+
+
+# ---------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser()
@@ -505,6 +610,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: the T x H x SM-budget sweep, one JSON line each")
+    ap.add_argument("--ceilings", action="store_true",
+                    help="instead of the bench line: bandwidth ceilings of plain streaming kernels")
     ap.add_argument("--only-main", action="store_true",
                     help="for profiling: only the all-SM timed loop (no 24-SM, fused, e2e or "
                          "decode passes)")
@@ -534,6 +641,11 @@ def main():
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     from combine_movement_gb300 import ep
+
+    if args.ceilings:
+        if rank == 0:
+            print(json.dumps(measure_ceilings(dev)), flush=True)
+        return
 
     if args.ncu_budgets:
         step = Step(ep, W.make_inputs(wl), dev)
