@@ -65,6 +65,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_combine.restype = i32
     lib.ep_get_dispatch_layout_noalloc.argtypes = [p, i64, i32, i32, p, p, p, p, p]
     lib.ep_get_dispatch_layout_noalloc.restype = i32
+    lib.ep_selftest_wait_timeout.argtypes = [p, ctypes.c_uint64, p]
+    lib.ep_selftest_wait_timeout.restype = i32
     lib.ep_get_status.argtypes = [p, p]
     lib.ep_get_status.restype = i32
     lib.ep_status_string.argtypes = [i32]
@@ -203,6 +205,11 @@ def ep_combine(expert_out: torch.Tensor, slot: torch.Tensor, topk_w: torch.Tenso
         _ptr(slot, torch.int32, "slot"), _ptr(topk_w, torch.float32, "topk_w"), T, H, K,
         _ptr(y, torch.bfloat16, "y"), _ptr(status, torch.int32, "status"), _stream(stream))
     _check(code, "ep_combine")
+
+
+def ep_selftest_wait_timeout(status: torch.Tensor, limit_ns: int, stream=None) -> None:
+    _check(lib.ep_selftest_wait_timeout(_ptr(status, torch.int32, "status"), int(limit_ns),
+                                        _stream(stream)), "ep_selftest_wait_timeout")
 
 
 def ep_get_status(status: torch.Tensor, stream=None) -> int:
