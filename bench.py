@@ -598,6 +598,107 @@ def measure_ceilings(dev) -> dict:
 
 
 # ---------------------------------------------------------------------------
+# overlap: data movement on n SMs next to arithmetic on the other SMs
+
+_SPIN_SRC = r"""
+#include <cuda_runtime.h>
+// ALU-bound stand-in for the experts' arithmetic: every thread runs a chain
+// of fp32 fmas; one CTA per SM (its shared-memory request forbids a second).
+__global__ void k_fma(float* out, int iters) {
+    float a = threadIdx.x * 1e-3f, b = 1.0f + blockIdx.x * 1e-6f, c = 0.5f, d = 0.25f;
+    for (int i = 0; i < iters; ++i) {
+        a = fmaf(a, b, c); c = fmaf(c, b, d); d = fmaf(d, b, a); b = fmaf(b, 0.999999f, 1e-7f);
+    }
+    if (a + c + d == 12345.0f) out[0] = a;
+}
+extern "C" int run_fma(void* out, int grid, int iters, void* stream) {
+    cudaFuncSetAttribute(k_fma, cudaFuncAttributeMaxDynamicSharedMemorySize, 120 * 1024);
+    k_fma<<<grid, 1024, 120 * 1024, (cudaStream_t)stream>>>((float*)out, iters);
+    return cudaGetLastError();
+}
+"""
+
+
+def run_overlap(ep, dev, budgets=(16, 24, 48), steps: int = 60) -> None:
+    """For each budget n: time (a) an ALU-bound kernel on 152-n SMs alone,
+    (b) `steps` dispatch+combine steps (DeepSeek-V3 prefill, layout done
+    beforehand) at budget n alone, (c) both at once on two streams. One JSON
+    line per budget, with the SM clock sampled during (c)."""
+    import ctypes
+    import tempfile
+    tmp = tempfile.mkdtemp(prefix="ep_overlap_")
+    src, so = os.path.join(tmp, "spin.cu"), os.path.join(tmp, "libspin.so")
+    with open(src, "w") as f:
+        f.write(_SPIN_SRC)
+    subprocess.run(["nvcc", "-O3", "-shared", "-Xcompiler", "-fPIC",
+                    "-gencode=arch=compute_103a,code=sm_103a", "-o", so, src], check=True)
+    L = ctypes.CDLL(so)
+    L.run_fma.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.zeros(1, device=dev)
+    step = Step(ep, W.make_inputs(W.DEEPSEEK_PREFILL), dev)
+    s_move = torch.cuda.Stream(dev, priority=-1)
+    s_comp = torch.cuda.Stream(dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def movement(n_steps):
+        for _ in range(n_steps):
+            step.dispatch(step.b, s_move)
+            step.combine(step.b, s_move)
+
+    for n in budgets:
+        ep.ep_set_num_sms(n)
+        grid = sms - n
+        with torch.cuda.stream(s_move):
+            movement(3)
+        torch.cuda.synchronize(dev)
+        # (b) movement alone
+        a0, a1 = ev(), ev()
+        a0.record(s_move)
+        movement(steps)
+        a1.record(s_move)
+        torch.cuda.synchronize(dev)
+        move_ms = a0.elapsed_time(a1)
+        # size the ALU kernel to last about as long as the movement
+        c0, c1 = ev(), ev()
+        c0.record(s_comp)
+        assert L.run_fma(out.data_ptr(), grid, 20000, s_comp.cuda_stream) == 0
+        c1.record(s_comp)
+        torch.cuda.synchronize(dev)
+        iters = max(20000, int(20000 * move_ms / max(c0.elapsed_time(c1), 1e-3)))
+        # (a) ALU alone
+        c0.record(s_comp)
+        L.run_fma(out.data_ptr(), grid, iters, s_comp.cuda_stream)
+        c1.record(s_comp)
+        torch.cuda.synchronize(dev)
+        comp_ms = c0.elapsed_time(c1)
+        # (c) both
+        sampler = ClockSampler(dev.index or 0)
+        sampler.__enter__()
+        c0.record(s_comp)
+        L.run_fma(out.data_ptr(), grid, iters, s_comp.cuda_stream)
+        c1.record(s_comp)
+        a0.record(s_move)
+        movement(steps)
+        a1.record(s_move)
+        torch.cuda.synchronize(dev)
+        sampler.__exit__(None, None, None)
+        flops = 4 * 2 * iters * 1024 * grid
+        print(json.dumps({
+            "num_sms_movement": n, "num_sms_alu": grid, "steps": steps,
+            "movement_ms_per_step_alone": round(move_ms / steps, 4),
+            "movement_ms_per_step_overlapped": round(a0.elapsed_time(a1) / steps, 4),
+            "alu_ms_alone": round(comp_ms, 3), "alu_ms_overlapped": round(c0.elapsed_time(c1), 3),
+            "alu_tflops_alone": round(flops / (comp_ms * 1e-3) / 1e12, 2),
+            "alu_tflops_overlapped": round(flops / (c0.elapsed_time(c1) * 1e-3) / 1e12, 2),
+            "clocks_overlapped": sampler.summary(),
+        }), flush=True)
+    ep.ep_set_num_sms(0)
+
+
+# ---------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser()
@@ -610,6 +711,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: the T x H x SM-budget sweep, one JSON line each")
+    ap.add_argument("--overlap", action="store_true",
+                    help="instead of the bench line: dispatch+combine on n SMs next to an "
+                         "ALU-bound kernel on the other SMs (n = 16, 24, 48)")
     ap.add_argument("--ceilings", action="store_true",
                     help="instead of the bench line: bandwidth ceilings of plain streaming kernels")
     ap.add_argument("--only-main", action="store_true",
@@ -641,6 +745,11 @@ def main():
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     from combine_movement_gb300 import ep
+
+    if args.overlap:
+        if rank == 0:
+            run_overlap(ep, dev)
+        return
 
     if args.ceilings:
         if rank == 0:
