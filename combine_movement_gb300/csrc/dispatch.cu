@@ -409,6 +409,8 @@ uint32_t dispatch_stage_capacity(int smem_optin, size_t reserve) {
     return static_cast<uint32_t>((per_warp / kStages) & ~static_cast<size_t>(15));
 }
 
+int dispatch_warps() { return kDispatchWarps; }
+
 cudaError_t launch_layout_dispatch(const DispatchArgs& a, FusedLayoutArgs f, int num_sms,
                                    cudaStream_t stream) {
     const size_t ring = static_cast<size_t>(barrier_region(kStages, kDispatchWarps)) +

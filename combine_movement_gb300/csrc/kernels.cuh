@@ -73,6 +73,9 @@ cudaError_t launch_layout_dispatch(const DispatchArgs& a, FusedLayoutArgs f, int
 // reserving `reserve` bytes for other shared data.
 uint32_t dispatch_stage_capacity(int smem_optin, size_t reserve);
 
+// Warps per dispatch CTA.
+int dispatch_warps();
+
 // ---- combine --------------------------------------------------------------
 
 struct CombineArgs {
