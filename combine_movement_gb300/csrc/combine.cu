@@ -105,9 +105,11 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
     int32_t s_lane = -1;
     float w_lane = 0.0f;
 
+    // (token, column block) of the current unit, advanced without divisions
+    int64_t t = u0 / n_cb;
+    uint32_t cb = static_cast<uint32_t>(u0 - t * n_cb);
     for (int64_t u = u0; u < u1; ++u) {
-        const int64_t t = u / n_cb;
-        const uint32_t col0 = static_cast<uint32_t>(u - t * n_cb) * kUnitBytes + lane * 16u;
+        const uint32_t col0 = cb * kUnitBytes + lane * 16u;
         if (t != tok) {
             tok = t;
             int32_t s = lane < K ? __ldg(a.slot + t * K + lane) : -1;
@@ -167,6 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
 #pragma unroll
         for (int j = 0; j < kUnroll; ++j)
             if (in_row[j]) st_v4(yrow + col0 + j * kColBytes, round8(acc[j]));
+        if (++cb == n_cb) {
+            cb = 0;
+            ++t;
+        }
     }
 }
 
