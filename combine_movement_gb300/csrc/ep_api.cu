@@ -159,7 +159,7 @@ size_t ep_layout_workspace_bytes(int64_t T, int K, int E) {
 int ep_layout_launches(int64_t T, int K, int E) {
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return -1;
     const ep::LayoutPlan p = ep::plan_layout(T * K, E);
-    if (p.num_tiles == 1 || p.coop) return 1;
+    if (p.num_tiles == 1 || p.cluster || p.coop) return 1;
     return p.num_tiles <= 512 ? 2 : 3;
 }
 

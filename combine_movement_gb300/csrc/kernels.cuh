@@ -17,6 +17,7 @@ struct LayoutPlan {
     int rounds;      // 32-entry rounds per warp per tile
     int64_t tile;    // entries per tile = warps * 32 * rounds
     int num_tiles;   // 1 => single fused launch, no workspace
+    bool cluster;    // one thread-block cluster (no workspace)
     bool coop;       // one cooperative launch (else tile + finish launches)
     size_t smem;     // dynamic shared memory of the tile kernels
     size_t counts_off;       // workspace byte offset of tile_counts (num_tiles > 1)

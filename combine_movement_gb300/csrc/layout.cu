@@ -112,14 +112,20 @@ __global__ void __launch_bounds__(1024) layout_tile_kernel(const int64_t* __rest
             bad |= (key[r] < 0 && v != -1);
         }
     }
+    // one pass: ranks within the warp and the warp's per-expert counts
+    int32_t rank[kMaxRounds];
     int32_t* my = run + static_cast<int64_t>(warp) * E;
     for (int e = lane; e < E; e += 32) my[e] = 0;
     __syncwarp();
 #pragma unroll
     for (int r = 0; r < kMaxRounds; ++r) {
+        rank[r] = 0;
         if (r < rounds) {
-            const uint32_t peers = peers_of(key[r], kbits);
-            if (key[r] >= 0 && lane == __ffs(peers) - 1) my[key[r]] += __popc(peers);
+            const int k = key[r];
+            const uint32_t peers = peers_of(k, kbits);
+            if (k >= 0) rank[r] = my[k] + __popc(peers & lanemask_lt());
+            __syncwarp();
+            if (k >= 0 && lane == __ffs(peers) - 1) my[k] += __popc(peers);
             __syncwarp();
         }
     }
@@ -152,23 +158,19 @@ __global__ void __launch_bounds__(1024) layout_tile_kernel(const int64_t* __rest
     }
     __syncthreads();
 
+    // my[] now holds each warp's first rank per expert (plus the expert's
+    // first row when FUSED)
 #pragma unroll
     for (int r = 0; r < kMaxRounds; ++r) {
-        if (r < rounds) {
-            const int64_t i = wbase + r * 32 + lane;
+        const int64_t i = wbase + r * 32 + lane;
+        if (r < rounds && i < N) {
             const int k = key[r];
-            const uint32_t peers = peers_of(k, kbits);
-            if (i < N) {
-                if (k >= 0) {
-                    const int32_t rank = my[k] + __popc(peers & lanemask_lt());
-                    slot[i] = FUSED ? rank : ((rank << kExpertBits) | k);
-                } else {
-                    slot[i] = -1;
-                }
+            if (k >= 0) {
+                const int32_t rk = my[k] + rank[r];
+                slot[i] = FUSED ? rk : ((rk << kExpertBits) | k);
+            } else {
+                slot[i] = -1;
             }
-            __syncwarp();
-            if (k >= 0 && lane == __ffs(peers) - 1) my[k] += __popc(peers);
-            __syncwarp();
         }
     }
 }
@@ -277,6 +279,139 @@ __global__ void __launch_bounds__(kFinishThreads) layout_finish_kernel(
     }
 }
 
+// ---- single-cluster layout ---------------------------------------------------
+// For tables that fit kClusterCtas tiles (up to 8 rounds per warp), one
+// thread-block cluster does the whole layout. Its CTAs are co-scheduled on
+// one GPC, so the tiles' per-expert counts are exchanged through distributed
+// shared memory and the hardware cluster barrier, with no global round trips
+// and no workspace:
+//   phase 1  as in the other kernels: ids, per-warp ranks and counts, tile
+//            counts into this CTA's shared memory
+//   barrier  (cluster)
+//   phase 2  every CTA reads each CTA's tile counts (DSMEM): expert totals and
+//            the rows of earlier tiles
+//   barrier  (cluster; after it no CTA reads another's shared memory, so each
+//            may finish and exit on its own)
+//   phase 3  scan across experts, final slots; CTA 0 writes counts, offsets.
+constexpr int kClusterCtas = 8;  // portable cluster size
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of `local` (this CTA's shared memory) in CTA `rank`
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ int32_t ld_cluster(uint32_t addr) {
+    int32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(1024) layout_cluster_kernel(
+    const int64_t* __restrict__ idx, int64_t N, int E, int rounds, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ slot, int32_t* status) {
+    extern __shared__ int32_t run[];  // [warps][E] per-warp counts, then [E] tile counts
+    griddep_wait();
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int tile_id = static_cast<int>(cluster_rank());
+    const int ntiles = static_cast<int>(gridDim.x);  // the grid is one cluster
+    const int64_t tile = static_cast<int64_t>(nwarps) * 32 * rounds;
+    const int64_t wbase = tile * tile_id + static_cast<int64_t>(warp) * 32 * rounds;
+    const int kbits = key_bits_for(E);
+    int32_t* tile_tot = run + static_cast<int64_t>(nwarps) * E;
+
+    int key[kMaxRounds];
+    int32_t rank[kMaxRounds];
+    bool bad = false;
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+        key[r] = -1;
+        rank[r] = 0;
+        const int64_t i = wbase + r * 32 + lane;
+        if (r < rounds && i < N) {
+            const int64_t v = __ldg(idx + i);
+            key[r] = expert_key(v, E);
+            bad |= (key[r] < 0 && v != -1);
+        }
+    }
+    if (bad) set_status(status, EP_ERR_BAD_EXPERT);
+    int32_t* my = run + static_cast<int64_t>(warp) * E;
+    for (int e = lane; e < E; e += 32) my[e] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+        if (r < rounds) {
+            const int k = key[r];
+            const uint32_t peers = peers_of(k, kbits);
+            if (k >= 0) rank[r] = my[k] + __popc(peers & lanemask_lt());
+            __syncwarp();
+            if (k >= 0 && lane == __ffs(peers) - 1) my[k] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    scan_across_warps(run, E, nwarps, tile_tot, 1);
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r)
+        if (r < rounds && key[r] >= 0) rank[r] += my[key[r]];
+    cluster_barrier();  // every CTA's tile counts are complete
+
+    // phase 2 (run[0 .. 2E) is free: ranks are in registers; tile_tot lies
+    // beyond it because there are at least 4 warps)
+    int32_t* tot = run;
+    int32_t* base = run + E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const uint32_t local = smem_u32(tile_tot + e);
+        int32_t c[kClusterCtas];
+#pragma unroll
+        for (int q = 0; q < kClusterCtas; ++q)
+            c[q] = q < ntiles ? ld_cluster(cluster_map(local, static_cast<uint32_t>(q))) : 0;
+        int32_t ts = 0, bs = 0;
+#pragma unroll
+        for (int q = 0; q < kClusterCtas; ++q) {
+            ts += c[q];
+            bs += q < tile_id ? c[q] : 0;
+        }
+        tot[e] = ts;
+        base[e] = bs;
+    }
+    cluster_barrier();  // no CTA reads another's shared memory after this
+
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, per * static_cast<int>(threadIdx.x)), e1 = min(E, e0 + per);
+    int64_t local = 0;
+    for (int e = e0; e < e1; ++e) local += tot[e];
+    int64_t total;
+    int64_t off = block_exclusive_scan(local, &total);
+    for (int e = e0; e < e1; ++e) {
+        if (tile_id == 0) {
+            offsets[e] = static_cast<int32_t>(off);
+            counts[e] = tot[e];
+        }
+        base[e] += static_cast<int32_t>(off);
+        off += tot[e];
+    }
+    if (tile_id == 0 && threadIdx.x == 0) offsets[E] = static_cast<int32_t>(total);
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+        const int64_t i = wbase + r * 32 + lane;
+        if (r < rounds && i < N) slot[i] = key[r] >= 0 ? base[key[r]] + rank[r] : -1;
+    }
+}
+
 // ---- single-launch layout (cooperative grid) -----------------------------------
 // For tables of up to kCoopMaxTiles tiles, one cooperative launch does what
 // the tile and finish kernels do, with one grid-wide barrier in between:
@@ -356,20 +491,11 @@ __global__ void __launch_bounds__(1024) layout_coop_kernel(const int64_t* __rest
         }
     }
     if (bad) set_status(status, EP_ERR_BAD_EXPERT);
+    // one pass: each entry's rank among its warp's earlier entries of the
+    // same expert, and the warp's per-expert counts
     int32_t* my = run + static_cast<int64_t>(warp) * E;
     for (int e = lane; e < E; e += 32) my[e] = 0;
     __syncwarp();
-#pragma unroll
-    for (int r = 0; r < kMaxRounds; ++r) {
-        if (r < rounds) {
-            const uint32_t peers = peers_of(key[r], kbits);
-            if (key[r] >= 0 && lane == __ffs(peers) - 1) my[key[r]] += __popc(peers);
-            __syncwarp();
-        }
-    }
-    __syncthreads();
-    scan_across_warps(run, E, nwarps, tile_counts + static_cast<int64_t>(tile_id) * E, 1);
-    __syncthreads();
 #pragma unroll
     for (int r = 0; r < kMaxRounds; ++r) {
         if (r < rounds) {
@@ -381,6 +507,13 @@ __global__ void __launch_bounds__(1024) layout_coop_kernel(const int64_t* __rest
             __syncwarp();
         }
     }
+    __syncthreads();
+    // counts -> each warp's first rank within the tile; tile totals published
+    scan_across_warps(run, E, nwarps, tile_counts + static_cast<int64_t>(tile_id) * E, 1);
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r)
+        if (r < rounds && key[r] >= 0) rank[r] += my[key[r]];
     if (!grid_barrier(sync + 1, nt, target)) {
         // leave the generation past every flag this call may have published
         if (threadIdx.x == 0) {
@@ -392,39 +525,48 @@ __global__ void __launch_bounds__(1024) layout_coop_kernel(const int64_t* __rest
     if (tile_id == 0 && threadIdx.x == 0) st_release_u64(sync, target);
 
     // phase 2: per expert, its total and the rows of earlier tiles. Q threads
-    // share an expert (tiles q, q+Q, ...); all of a thread's loads are in
-    // flight at once; order-free integer adds combine the Q partial sums.
-    int32_t* tot = run;       // [E]
-    int32_t* base = run + E;  // [E]
-    for (int e = threadIdx.x; e < E; e += blockDim.x) tot[e] = base[e] = 0;
+    // share an expert (tiles q, q+Q, ...), each with all its loads in flight
+    // at once; partial sums go to shared memory and one thread per expert
+    // adds them up. No atomics.
     __syncthreads();
-    {
-        const int Q = blockDim.x >= E ? static_cast<int>(blockDim.x) / E : 1;
-        for (int x = threadIdx.x; x < E * Q; x += blockDim.x) {
-            const int e = x % E, q = x / E;
-            int32_t t_sum = 0, b_sum = 0;
-            for (int t0 = q; t0 < nt; t0 += 16 * Q) {
-                int32_t c[16];
+    const int Q = max(1, min(static_cast<int>(blockDim.x) / E, nwarps / 2));
+    int32_t* part_t = run;                              // [Q][E] totals
+    int32_t* part_b = run + static_cast<int64_t>(Q) * E;  // [Q][E] earlier tiles
+    for (int x = threadIdx.x; x < E * Q; x += blockDim.x) {
+        const int e = x % E, q = x / E;
+        int32_t t_sum = 0, b_sum = 0;
+        for (int t0 = q; t0 < nt; t0 += 16 * Q) {
+            int32_t c[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int t = t0 + u * Q;
-                    c[u] = t < nt ? __ldcg(tile_counts + static_cast<int64_t>(t) * E + e) : 0;
-                }
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    t_sum += c[u];
-                    b_sum += (t0 + u * Q < tile_id) ? c[u] : 0;
-                }
+            for (int u = 0; u < 16; ++u) {
+                const int t = t0 + u * Q;
+                c[u] = t < nt ? __ldcg(tile_counts + static_cast<int64_t>(t) * E + e) : 0;
             }
-            if (t_sum != 0) atomicAdd(&tot[e], t_sum);
-            if (b_sum != 0) atomicAdd(&base[e], b_sum);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                t_sum += c[u];
+                b_sum += (t0 + u * Q < tile_id) ? c[u] : 0;
+            }
         }
+        part_t[static_cast<int64_t>(q) * E + e] = t_sum;
+        part_b[static_cast<int64_t>(q) * E + e] = b_sum;
     }
     __syncthreads();
+    int32_t* tot = part_t;   // row 0 receives the sums
+    int32_t* base = part_b;
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = min(E, per * static_cast<int>(threadIdx.x)), e1 = min(E, e0 + per);
     int64_t local = 0;
-    for (int e = e0; e < e1; ++e) local += tot[e];
+    for (int e = e0; e < e1; ++e) {
+        int32_t ts = 0, bs = 0;
+        for (int q = 0; q < Q; ++q) {
+            ts += part_t[static_cast<int64_t>(q) * E + e];
+            bs += part_b[static_cast<int64_t>(q) * E + e];
+        }
+        tot[e] = ts;
+        base[e] = bs;
+        local += ts;
+    }
     int64_t total;
     int64_t off = block_exclusive_scan(local, &total);
     for (int e = e0; e < e1; ++e) {
@@ -463,6 +605,17 @@ LayoutPlan plan_layout(int64_t N, int E) {
     p.tile = per_round * p.rounds;
     if (N > per_round * kFusedRounds) p.num_tiles = static_cast<int>((N + p.tile - 1) / p.tile);
     p.smem = sizeof(int32_t) * static_cast<size_t>(E) * warps;
+    // one cluster when the table fits kClusterCtas tiles of <= 8 rounds
+    p.cluster = p.num_tiles > 1 && N <= per_round * kClusterCtas * kMaxRounds;
+    if (p.cluster) {
+        p.rounds = static_cast<int>((N + per_round * kClusterCtas - 1) / (per_round * kClusterCtas));
+        p.tile = per_round * p.rounds;
+        p.num_tiles = static_cast<int>((N + p.tile - 1) / p.tile);
+        p.smem = sizeof(int32_t) * static_cast<size_t>(E) * (warps + 1);
+        p.workspace_bytes = 0;
+        p.coop = false;
+        return p;
+    }
     p.coop = p.num_tiles > 1 && p.num_tiles <= kCoopMaxTiles;
     if (p.num_tiles > 1) {
         // [generation][flag x tiles] | tile_counts[tiles][E]
@@ -500,6 +653,26 @@ cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,
         return launch_dependent(layout_tile_kernel<true>, 1, threads, p.smem, stream, idx, N, E,
                                 p.rounds, 1, static_cast<int32_t*>(nullptr), counts, offsets,
                                 slot, status);
+    }
+    if (p.cluster) {
+        cudaError_t err = cudaFuncSetAttribute(layout_cluster_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(p.smem));
+        if (err != cudaSuccess) return err;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles));
+        cfg.blockDim = dim3(static_cast<unsigned>(threads));
+        cfg.dynamicSmemBytes = p.smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(p.num_tiles);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, idx, N, E, p.rounds, counts, offsets,
+                                  slot, status);
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint64_t* sync = reinterpret_cast<uint64_t*>(ws);

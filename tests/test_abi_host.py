@@ -65,7 +65,8 @@ def test_status_strings(ep):
 
 def test_workspace_bytes(ep):
     assert ep.ep_layout_workspace_bytes(128, 8, 256) == 0          # one fused launch
-    big = ep.ep_layout_workspace_bytes(4096, 8, 256)
+    assert ep.ep_layout_workspace_bytes(4096, 8, 256) == 0         # one thread-block cluster
+    big = ep.ep_layout_workspace_bytes(16384, 8, 128)              # grid-wide cooperative launch
     assert big > 0 and big % 4 == 0
     assert big % 4 == 0 and big > 4 * 256 * 2                        # barrier words, totals, E x tiles
     assert ep.ep_layout_workspace_bytes(4096, 33, 256) == 0        # invalid -> 0
@@ -74,7 +75,8 @@ def test_workspace_bytes(ep):
 
 def test_layout_launch_counts(ep):
     assert ep.ep_layout_launches(128, 8, 256) == 1       # one tile: fused block
-    assert ep.ep_layout_launches(4096, 8, 256) == 1      # few tiles: one cooperative launch
+    assert ep.ep_layout_launches(4096, 8, 256) == 1      # one thread-block cluster
+    assert ep.ep_layout_launches(16384, 8, 128) == 1     # one cooperative launch
     assert ep.ep_layout_launches(20000, 8, 4096) == 2    # many tiles: tile + finish launches
     assert ep.ep_layout_launches(10, 33, 8) == -1
 
@@ -106,8 +108,10 @@ def test_host_argument_checks(ep):
     assert lib.ep_get_dispatch_layout(A, 4, 2, 0, A, A, A, None, 0, None, None) == ep.EP_ERR_INVALID
     assert lib.ep_get_dispatch_layout(A, 4, 2, 5000, A, A, A, None, 0, None, None) == ep.EP_ERR_UNSUPPORTED
     assert lib.ep_get_dispatch_layout(A + 4, 4, 2, 8, A, A, A, None, 0, None, None) == ep.EP_ERR_INVALID
-    assert lib.ep_get_dispatch_layout(A, 4096, 8, 256, A, A, A, None, 0, None, None) == ep.EP_ERR_WORKSPACE
-    assert lib.ep_get_dispatch_layout(A, 4096, 8, 256, A, A, A, A, 64, None, None) == ep.EP_ERR_WORKSPACE
+    # a table that needs a workspace: missing or too small is refused before any launch
+    assert ep.ep_layout_workspace_bytes(16384, 8, 128) > 64
+    assert lib.ep_get_dispatch_layout(A, 16384, 8, 128, A, A, A, None, 0, None, None) == ep.EP_ERR_WORKSPACE
+    assert lib.ep_get_dispatch_layout(A, 16384, 8, 128, A, A, A, A, 64, None, None) == ep.EP_ERR_WORKSPACE
     assert lib.ep_get_status(None, None) == ep.EP_ERR_INVALID
     # fused layout + dispatch
     ld = lib.ep_layout_dispatch
