@@ -417,6 +417,12 @@ class _Flusher:
         self.buf.zero_()
 
 
+def spread(ms: list) -> list:
+    """Median, 10th and 90th percentile of per-call event times, in µs."""
+    q = statistics.quantiles([1e3 * v for v in ms], n=10)
+    return [round(1e3 * statistics.median(ms), 2), round(q[0], 2), round(q[-1], 2)]
+
+
 def time_call(fn, reps: int, flush=None) -> float:
     """Median microseconds of fn() on the current stream (CUDA events). The
     GPU is kept busy (L2 flush, or a short spin) while the host enqueues the
@@ -538,6 +544,78 @@ __global__ void k_bulk_write(uint8_t* dst, size_t nbytes) {
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
 }
+// Stage probes for the two-stage pipeline model of the dispatch ring: the
+// same per-warp ring shape (4 stages, 2 loads ahead, one elected lane, the
+// same chunk and units per warp) doing only its load stage or only its store
+// stage, over buffers of their own. Every mbarrier wait gives up after 2 s
+// and records it in *err; after a give-up the lane still waits (bounded) for
+// the loads it issued, so no copy lands in shared memory after the CTA ends.
+constexpr int kNS = 4, kP = 2;
+__device__ __forceinline__ bool probe_wait(uint32_t bar, uint32_t parity) {
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    while (true) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+        uint64_t t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 > 2000000000ull) return false;
+    }
+}
+__host__ __device__ constexpr uint32_t ring_region(int warps) { return (8u * kNS * warps + 127u) & ~127u; }
+__global__ void k_ring_load(const uint8_t* src, long long units, uint32_t chunk, int* err) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
+    if (lane != 0) return;
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(sm);
+    const uint32_t bar0 = base + 8u * kNS * warp;
+    const uint32_t buf0 = base + ring_region(nw) + kNS * chunk * warp;
+    for (int s = 0; s < kNS; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar0 + 8u * s) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const long long W = (long long)gridDim.x * nw, gw = (long long)blockIdx.x * nw + warp;
+    const long long u0 = units * gw / W, n = units * (gw + 1) / W - u0;
+    long long issued = 0;
+    auto issue = [&]() {
+        const int s = (int)(issued % kNS);
+        const uint32_t bar = bar0 + 8u * s;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(chunk) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     :: "r"(buf0 + s * chunk), "l"(src + (u0 + issued) * (long long)chunk), "r"(chunk), "r"(bar) : "memory");
+        ++issued;
+    };
+    while (issued < kP && issued < n) issue();
+    for (long long j = 0; j < n; ++j) {
+        if (issued < n) issue();  // its stage was last used by unit issued-kNS < j, already waited
+        if (!probe_wait(bar0 + 8u * (j % kNS), (uint32_t)((j / kNS) & 1))) {
+            atomicExch(err, 1);
+            for (long long q = j + 1; q < issued; ++q) probe_wait(bar0 + 8u * (q % kNS), (uint32_t)((q / kNS) & 1));
+            return;
+        }
+    }
+}
+__global__ void k_ring_store(uint8_t* dst, long long units, uint32_t chunk, int K) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
+    uint8_t* mine = sm + ring_region(nw) + (size_t)kNS * chunk * warp;
+    for (uint32_t i = lane; i < kNS * chunk / 4; i += 32) reinterpret_cast<uint32_t*>(mine)[i] = i;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane != 0) return;
+    const uint32_t buf0 = (uint32_t)__cvta_generic_to_shared(mine);
+    const long long W = (long long)gridDim.x * nw, gw = (long long)blockIdx.x * nw + warp;
+    const long long u0 = units * gw / W, n = units * (gw + 1) / W - u0;
+    for (long long j = 0; j < n; ++j) {
+        asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(kNS - kP - 1) : "memory");
+        const uint32_t src = buf0 + (uint32_t)(j % kNS) * chunk;
+        for (int k = 0; k < K; ++k)
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                         :: "l"(dst + ((u0 + j) * K + k) * (long long)chunk), "r"(src), "r"(chunk) : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 extern "C" {
 int bw_write(void* p, size_t n, int grid, int block) { k_write<<<grid, block>>>((uint4*)p, n / 16); return cudaGetLastError(); }
 int bw_read(void* p, size_t n, void* sink, int grid, int block) { k_read<<<grid, block>>>((const uint4*)p, n / 16, (uint32_t*)sink); return cudaGetLastError(); }
@@ -545,8 +623,93 @@ int bw_copy(void* a, void* b, size_t n, int grid, int block) { k_copy<<<grid, bl
 int bw_bulk_write(void* p, size_t n, int grid, int warps) {
     cudaFuncSetAttribute(k_bulk_write, cudaFuncAttributeMaxDynamicSharedMemorySize, warps * 8192);
     k_bulk_write<<<grid, warps * 32, warps * 8192>>>((uint8_t*)p, n); return cudaGetLastError(); }
+int ring_smem(int warps, unsigned chunk) { return (int)(ring_region(warps) + (size_t)kNS * chunk * warps); }
+int ring_load(const void* src, long long units, unsigned chunk, int grid, int warps, int* err) {
+    const int smem = ring_smem(warps, chunk);
+    cudaError_t e = cudaFuncSetAttribute(k_ring_load, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k_ring_load<<<grid, warps * 32, smem>>>((const uint8_t*)src, units, chunk, err); return cudaGetLastError(); }
+int ring_store(void* dst, long long units, unsigned chunk, int K, int grid, int warps) {
+    const int smem = ring_smem(warps, chunk);
+    cudaError_t e = cudaFuncSetAttribute(k_ring_store, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k_ring_store<<<grid, warps * 32, smem>>>((uint8_t*)dst, units, chunk, K); return cudaGetLastError(); }
 }
 """
+
+
+def _probe_lib():
+    """The probes above, built with nvcc into a temporary directory."""
+    import ctypes
+    import tempfile
+    tmp = tempfile.mkdtemp(prefix="ep_probes_")
+    src, so = os.path.join(tmp, "bw.cu"), os.path.join(tmp, "libbw.so")
+    with open(src, "w") as f:
+        f.write(_CEILING_SRC)
+    subprocess.run(["nvcc", "-O3", "-shared", "-Xcompiler", "-fPIC",
+                    "-gencode=arch=compute_103a,code=sm_103a", "-o", so, src], check=True)
+    return ctypes.CDLL(so)
+
+
+def pipeline_time(n: int, t_load: float, t_store: float) -> float:
+    """Two-stage pipeline closed form ("tensor-memory-accelerator" atlas page,
+    Science and assumptions): the first unit pays both stages, each of the
+    other n-1 units one interval of the slower stage."""
+    return 0.0 if n <= 0 else t_load + t_store + (n - 1) * max(t_load, t_store)
+
+
+def run_pipeline_model(ep, dev, wl: W.Workload, budgets=(0, 24, 16)) -> None:
+    """Model dispatch as the two-stage pipeline its ring implements and
+    compare with the measured kernel. Per SM budget: time the ring's load
+    stage alone and its store stage alone (same ring shape, chunk, units per
+    warp; probes above), take per-unit stage times t = stage time / N with
+    N = units per warp, and print the closed form, the serial sum and the
+    measured dispatch time (all cold L2, medians). One JSON line per budget."""
+    import ctypes
+    L = _probe_lib()
+    step = Step(ep, W.make_inputs(wl), dev)
+    flush = _Flusher(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    sms_all = torch.cuda.get_device_properties(dev).multi_processor_count
+    warps = 8  # warps per dispatch CTA in the library's build
+    row = 2 * wl.H
+    for b in budgets:
+        ep.ep_set_num_sms(b)
+        grid = min(b or sms_all, sms_all)
+        chunk = ep.ep_dispatch_chunk_bytes(wl.T, wl.H, wl.K)
+        if chunk <= 0:
+            raise SystemExit("ep_dispatch_chunk_bytes failed")
+        n_chunks = -(-row // chunk)
+        units = wl.T * n_chunks
+        src = torch.empty(units * chunk, dtype=torch.uint8, device=dev)
+        dst = torch.empty(units * wl.K * chunk, dtype=torch.uint8, device=dev)
+        vp, ll, u32 = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_uint
+        errp = ctypes.cast(err.data_ptr(), ctypes.POINTER(ctypes.c_int))
+
+        def load():
+            if L.ring_load(vp(src.data_ptr()), ll(units), u32(chunk), grid, warps, errp) != 0:
+                raise SystemExit("ring load probe: launch failed")
+
+        def store():
+            if L.ring_store(vp(dst.data_ptr()), ll(units), u32(chunk), wl.K, grid, warps) != 0:
+                raise SystemExit("ring store probe: launch failed")
+
+        t_load = time_call(load, 20, flush)
+        t_store = time_call(store, 20, flush)
+        t_disp = time_call(lambda: step.dispatch(step.b), 20, flush)
+        if int(err.item()) != 0:
+            raise SystemExit("ring load probe: a wait gave up")
+        n = -(-units // (grid * warps))
+        model = pipeline_time(n, t_load / n, t_store / n)
+        print(json.dumps({
+            "workload": wl.name, "num_sms": grid, "chunk_bytes": chunk, "units_per_warp": n,
+            "load_stage_us": round(t_load, 1), "store_stage_us": round(t_store, 1),
+            "model_pipelined_us": round(model, 1), "model_serial_us": round(t_load + t_store, 1),
+            "dispatch_us": round(t_disp, 1), "dispatch_over_model": round(t_disp / model, 3),
+        }), flush=True)
+        del src, dst
+        torch.cuda.empty_cache()
+    ep.ep_set_num_sms(0)
 
 
 def measure_ceilings(dev) -> dict:
@@ -554,14 +717,7 @@ def measure_ceilings(dev) -> dict:
     (16-byte vectors; 8 KB bulk stores), all SMs and 24 SMs, plus pinned
     host<->device copy rates. Built from the source above with nvcc."""
     import ctypes
-    import tempfile
-    tmp = tempfile.mkdtemp(prefix="ep_ceilings_")
-    src, so = os.path.join(tmp, "bw.cu"), os.path.join(tmp, "libbw.so")
-    with open(src, "w") as f:
-        f.write(_CEILING_SRC)
-    subprocess.run(["nvcc", "-O3", "-shared", "-Xcompiler", "-fPIC",
-                    "-gencode=arch=compute_103a,code=sm_103a", "-o", so, src], check=True)
-    L = ctypes.CDLL(so)
+    L = _probe_lib()
     vp, sz = ctypes.c_void_p, ctypes.c_size_t
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     n = 1 << 30
@@ -714,6 +870,8 @@ def main():
     ap.add_argument("--overlap", action="store_true",
                     help="instead of the bench line: dispatch+combine on n SMs next to an "
                          "ALU-bound kernel on the other SMs (n = 16, 24, 48)")
+    ap.add_argument("--pipeline-model", action="store_true",
+                    help="two-stage pipeline model of the dispatch ring vs the measured kernel")
     ap.add_argument("--ceilings", action="store_true",
                     help="instead of the bench line: bandwidth ceilings of plain streaming kernels")
     ap.add_argument("--only-main", action="store_true",
@@ -749,6 +907,11 @@ def main():
     if args.overlap:
         if rank == 0:
             run_overlap(ep, dev)
+        return
+
+    if args.pipeline_model:
+        if rank == 0:
+            run_pipeline_model(ep, dev, wl)
         return
 
     if args.ceilings:
@@ -817,6 +980,8 @@ def main():
             "dispatch_us": 1e3 * d, "combine_us": 1e3 * c, "layout_us": 1e3 * lay,
             "dispatch_gbs": ab["dispatch"] / (d * 1e-3) / 1e9,
             "combine_gbs": ab["combine"] / (c * 1e-3) / 1e9,
+            "us_median_p10_p90": {k: spread(run[f"{k}_ms"])
+                                  for k in ("layout", "dispatch", "combine")},
         }
 
     def summarize_fused(run: dict, nsms: int) -> dict:

@@ -163,6 +163,19 @@ int ep_layout_launches(int64_t T, int K, int E) {
     return p.num_tiles <= 512 ? 2 : 3;
 }
 
+int64_t ep_dispatch_chunk_bytes(int64_t T, int64_t H, int K) {
+    if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || H * 2 > 0x7FFFFFF0 ||
+        T * static_cast<int64_t>(K) >= (int64_t{1} << 31))
+        return -1;
+    int sm_count = 0, smem_optin = 0;
+    if (!device_limits(&sm_count, &smem_optin)) return -1;
+    ep::DispatchArgs a{};
+    if (plan_dispatch(&a, nullptr, T, H, K, nullptr, nullptr, 0, nullptr, nullptr, nullptr,
+                      nullptr, smem_optin, 0, sms_in_effect(sm_count)) != EP_OK)
+        return -1;
+    return a.chunk_bytes;
+}
+
 ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, int E,
                                    int32_t* counts, int32_t* offsets, int32_t* slot,
                                    void* workspace, size_t workspace_bytes, int32_t* status,

@@ -113,6 +113,13 @@ EP_API size_t ep_layout_workspace_bytes(int64_t T, int K, int E);
  * invalid sizes. */
 EP_API int ep_layout_launches(int64_t T, int K, int E);
 
+/* Bytes per row chunk that ep_dispatch would use for these sizes at the
+ * current SM budget on the current device: each bf16 row of 2*H bytes is cut
+ * into equal 16-byte-multiple chunks, each one bulk load and K bulk stores
+ * (one ring unit). For measurements that model the ring; -1 for invalid
+ * sizes or when the device cannot be queried. */
+EP_API int64_t ep_dispatch_chunk_bytes(int64_t T, int64_t H, int K);
+
 /* Layout (per-expert histogram, exclusive prefix sums and per-(token,k)
  * destination slot).
  *   topk_idx   int64 [T][K]   routing table (DeepEP's topk_idx)

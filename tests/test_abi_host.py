@@ -81,6 +81,32 @@ def test_layout_launch_counts(ep):
     assert ep.ep_layout_launches(10, 33, 8) == -1
 
 
+def test_dispatch_chunk_bytes_rejects_invalid_sizes(ep):
+    assert ep.ep_dispatch_chunk_bytes(4096, 7166, 8) == -1   # H % 8 != 0
+    assert ep.ep_dispatch_chunk_bytes(4096, 7168, 33) == -1  # K above the limit
+    assert ep.ep_dispatch_chunk_bytes(-1, 7168, 8) == -1
+    assert ep.ep_dispatch_chunk_bytes(1 << 28, 7168, 8) == -1  # T*K overflows int32 slots
+
+
+@pytest.mark.gpu
+def test_dispatch_chunk_bytes_plan(ep):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    try:
+        ep.ep_set_num_sms(0)
+        # prefill rows of 14336 B: two 7168-B chunks fill the ring's stages
+        assert ep.ep_dispatch_chunk_bytes(4096, 7168, 8) == 7168
+        # a decode batch is cut finer so every warp gets work, never below 512 B
+        c = ep.ep_dispatch_chunk_bytes(128, 7168, 8)
+        assert c % 16 == 0 and 512 <= c < 7168
+        ep.ep_set_num_sms(24)
+        c24 = ep.ep_dispatch_chunk_bytes(128, 7168, 8)
+        assert c24 % 16 == 0 and c <= c24 <= 7168
+    finally:
+        ep.ep_set_num_sms(0)
+
+
 def _raw(ep):
     return ep.lib
 
