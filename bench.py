@@ -425,14 +425,15 @@ def spread(ms: list) -> list:
 
 def time_call(fn, reps: int, flush=None) -> float:
     """Median microseconds of fn() on the current stream (CUDA events). The
-    GPU is kept busy (L2 flush, or a short spin) while the host enqueues the
-    call, so host launch overhead is not counted."""
+    GPU is kept busy (L2 flush, or a ~100 us spin, longer than the host takes
+    to enqueue a step through the Python binding) while the host enqueues
+    the call, so host launch overhead is not counted."""
     ts = []
     for i in range(reps + 3):
         if flush is not None:
             flush()
         else:
-            torch.cuda._sleep(40000)
+            torch.cuda._sleep(200000)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()

@@ -41,6 +41,11 @@ namespace {
 constexpr size_t kRunSmemBudget = 64 * 1024;  // per-warp expert counters of the tile kernel
 constexpr int kMaxRounds = 8;                 // 32-entry rounds per warp per tile, at most
 constexpr int kFusedRounds = 1;               // one block alone up to this many rounds
+#ifndef EP_LAYOUT_SINGLE_ROUNDS
+#define EP_LAYOUT_SINGLE_ROUNDS 4
+#endif
+constexpr int kSingleRounds = EP_LAYOUT_SINGLE_ROUNDS;  // target rounds per warp then
+static_assert(kSingleRounds >= 1 && kSingleRounds <= 8, "single-block rounds in [1, 8]");
 constexpr int kTargetTiles = 128;             // tiles to aim for before rounds grow
 constexpr int kMaxRedundantTiles = 512;       // above this, one block scans for everyone
 constexpr int kCoopMaxTiles = 128;            // tables of at most this many tiles: one launch
@@ -595,15 +600,24 @@ LayoutPlan plan_layout(int64_t N, int E) {
     p.warps = warps;
     const int64_t per_round = 32LL * warps;  // entries per round of the whole block
     if (N <= per_round * kFusedRounds) {
+        // one block: as few warps as give each about kSingleRounds rounds
         p.num_tiles = 1;
-        p.rounds = static_cast<int>((N + per_round - 1) / per_round);
+        int64_t w = (N + 32LL * kSingleRounds - 1) / (32LL * kSingleRounds);
+        w = w < 1 ? 1 : (w > warps ? warps : w);
+        warps = static_cast<int>(w);
+        p.warps = warps;
+        const int64_t pr = 32LL * warps;
+        p.rounds = static_cast<int>((N + pr - 1) / pr);
         if (p.rounds < 1) p.rounds = 1;
+        p.tile = pr * p.rounds;
+        p.smem = sizeof(int32_t) * static_cast<size_t>(E) * warps;
+        return p;
     } else {
         int64_t r = (N + per_round * kTargetTiles - 1) / (per_round * kTargetTiles);
         p.rounds = static_cast<int>(r < 1 ? 1 : (r > kMaxRounds ? kMaxRounds : r));
     }
     p.tile = per_round * p.rounds;
-    if (N > per_round * kFusedRounds) p.num_tiles = static_cast<int>((N + p.tile - 1) / p.tile);
+    p.num_tiles = static_cast<int>((N + p.tile - 1) / p.tile);
     p.smem = sizeof(int32_t) * static_cast<size_t>(E) * warps;
     // one cluster when the table fits kClusterCtas tiles of <= 8 rounds
     p.cluster = p.num_tiles > 1 && N <= per_round * kClusterCtas * kMaxRounds;
