@@ -289,6 +289,59 @@ def test_side_stream_and_repeat_determinism(ep):
         assert np.array_equal(a[k], b[k], equal_nan=True)
 
 
+def test_back_to_back_batches_share_buffers_on_one_stream(ep):
+    """Several batches through the same device buffers on one stream with no
+    host synchronisation between them. Every kernel is launched with
+    programmatic dependent launch and may start while the previous one
+    finishes, so this checks that each still sees its producer's writes
+    (slot, recv_x, the expert stand-in's output) and that no kernel of a
+    batch overwrites what a kernel of the previous batch still reads."""
+    dev = torch.device("cuda:0")
+    T, H, E, K = 1536, 1032, 64, 6
+    cases = [(11, "uniform", 0.0, 1.5), (12, "zipf", 0.1, 1.0),
+             (13, "uniform", 0.2, 1.5), (14, "zipf", 0.0, 1.0)]
+    inps = [_custom(T, H, E, K, seed=sd, mask=m, routing=r) for sd, r, m, _ in cases]
+    refs = [oracle_path(inp, T * K, sc) for inp, (_, _, _, sc) in zip(inps, cases)]
+    idx = [inp.topk_idx.to(dev) for inp in inps]
+    w = [inp.topk_w.to(dev) for inp in inps]
+    x = [inp.x.to(dev) for inp in inps]
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    nws = ep.ep_layout_workspace_bytes(T, K, E)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev) if nws else None
+    recv = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+    eo = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = [dict(slot=torch.empty((T, K), dtype=torch.int32).pin_memory(),
+                offsets=torch.empty(E + 1, dtype=torch.int32).pin_memory(),
+                recv=torch.empty((T * K, H), dtype=torch.bfloat16).pin_memory(),
+                y=torch.empty((T, H), dtype=torch.bfloat16).pin_memory()) for _ in cases]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for b in (0, 24):
+        ep.ep_set_num_sms(b)
+        with torch.cuda.stream(s):
+            for i, (_, _, _, sc) in enumerate(cases):
+                ep.ep_get_dispatch_layout(idx[i], E, counts, offsets, slot, ws, status, s)
+                ep.ep_dispatch(x[i], slot, recv, None, None, None, status, s)
+                eo.copy_(W.expert_standin(recv, sc))
+                ep.ep_combine(eo, slot, w[i], y, status, s)
+                for name, src in (("slot", slot), ("offsets", offsets), ("recv", recv), ("y", y)):
+                    out[i][name].copy_(src, non_blocking=True)
+        s.synchronize()
+        assert ep.ep_get_status(status) == ep.EP_OK
+        for i, ref in enumerate(refs):
+            assert np.array_equal(out[i]["slot"].numpy(), ref.slot), f"batch {i}: slot"
+            assert np.array_equal(out[i]["offsets"].numpy(), ref.offsets), f"batch {i}: offsets"
+            r = bits(out[i]["recv"])
+            valid = int(ref.offsets[-1])
+            assert np.array_equal(r[:valid], ref.recv_x[:valid]), f"batch {i}: recv_x"
+            assert np.array_equal(bits(out[i]["y"]), ref.y), f"batch {i}: y"
+    ep.ep_set_num_sms(0)
+
+
 # ---- ep_layout_dispatch: layout and dispatch in one launch -----------------
 
 @pytest.mark.parametrize("name,budgets", [
