@@ -17,6 +17,10 @@
 // then issues K independent 16-byte loads (read-only path, no L1 allocation),
 // widens bf16 to fp32 exactly (bit shift), runs the fma chain in k order and
 // writes 16 bytes, so every warp store is a coalesced 512-byte row segment.
+// Units whose K slots are all valid and which lie wholly inside the row take
+// an unpredicated body whose fmas go in packed fp32 pairs (fma.rn.f32x2,
+// the same rounding per element); the wide shape always has it, the narrow
+// one up to K = 6.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -41,6 +45,11 @@ namespace {
 #endif
 #ifndef EP_COMBINE_NARROW_UNROLL
 #define EP_COMBINE_NARROW_UNROLL 1
+#endif
+// The narrow shape takes the unpredicated fast path (below) only up to this
+// K: with more rows per unit its registers spill at 768 threads.
+#ifndef EP_COMBINE_NARROW_FAST_MAX_K
+#define EP_COMBINE_NARROW_FAST_MAX_K 6
 #endif
 // Budgets of at least this many SMs use the wide shape.
 #ifndef EP_COMBINE_WIDE_MIN_SMS
@@ -68,6 +77,20 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4& v) {
     }
 }
 
+// Same arithmetic as fma8 with packed fp32 pairs: acc2[i] holds elements
+// 2i and 2i+1; fma.rn.f32x2 rounds each half exactly like fmaf.
+__device__ __forceinline__ void fma8_x2(uint64_t (&acc2)[4], float w, const uint4& v) {
+    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+    uint64_t w2;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(w2) : "f"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint64_t e2;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(e2) : "r"(q[i] << 16), "r"(q[i] & 0xFFFF0000u));
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[i]) : "l"(w2), "l"(e2));
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -82,7 +105,7 @@ __device__ __forceinline__ uint4 round8(const float (&acc)[8]) {
 // registers). KT == 0: any K <= 32, broadcast per unit. A unit is UN
 // consecutive 512-byte column blocks of one token, so each lane keeps
 // UN * K independent 16-byte loads in flight.
-template <int KT, int kThreads, int kUnroll>
+template <int KT, int kThreads, int kUnroll, bool kFast>
 __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs a) {
     griddep_wait();
     griddep_launch_dependents();
@@ -102,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
     const uint8_t* rowp[KR];
     float wk[KR];
     bool on[KR];
+    bool all_on = false;  // every one of the token's K slots is valid (warp-uniform)
     int32_t s_lane = -1;
     float w_lane = 0.0f;
 
@@ -128,7 +152,38 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
                     on[k] = sk >= 0;
                     rowp[k] = a.expert_out + static_cast<int64_t>(sk < 0 ? 0 : sk) * a.row_bytes;
                 }
+                all_on = __all_sync(kFullMask, lane >= K || s >= 0);
             }
+        }
+        // kFast, common case: no masked slot and the whole unit inside the
+        // row, so loads and fmas need no per-element predicates, and the fmas
+        // go in packed pairs.
+        if (kFast && KT > 0 && all_on && (cb + 1) * kUnitBytes <= a.row_bytes) {
+            uint4 v[kUnroll][KR];
+#pragma unroll
+            for (int k = 0; k < KR; ++k)
+#pragma unroll
+                for (int j = 0; j < kUnroll; ++j) v[j][k] = ld_expert(rowp[k] + col0 + j * kColBytes);
+            float acc[kUnroll][8];
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j) {
+                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f pairs
+#pragma unroll
+                for (int k = 0; k < KR; ++k) fma8_x2(acc2, wk[k], v[j][k]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    asm("mov.b64 {%0, %1}, %2;"
+                        : "=f"(acc[j][2 * i]), "=f"(acc[j][2 * i + 1])
+                        : "l"(acc2[i]));
+            }
+            uint8_t* yrow = a.y + t * static_cast<int64_t>(a.row_bytes);
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j) st_v4(yrow + col0 + j * kColBytes, round8(acc[j]));
+            if (++cb == n_cb) {
+                cb = 0;
+                ++t;
+            }
+            continue;
         }
         float acc[kUnroll][8];
 #pragma unroll
@@ -176,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
     }
 }
 
-template <int KT, int kThreads, int kUnroll>
+template <int KT, int kThreads, int kUnroll, bool kFast>
 cudaError_t launch_shape(const CombineArgs& a, int num_sms, cudaStream_t stream) {
     constexpr uint32_t kUnitBytes = kColBytes * kUnroll;
     const int64_t units = a.T * ((a.row_bytes + kUnitBytes - 1) / kUnitBytes);
@@ -184,7 +239,7 @@ cudaError_t launch_shape(const CombineArgs& a, int num_sms, cudaStream_t stream)
     const int64_t ctas_needed = (units + warps_per_cta - 1) / warps_per_cta;
     const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
     if (grid <= 0) return cudaSuccess;
-    auto kern = combine_kernel<KT, kThreads, kUnroll>;
+    auto kern = combine_kernel<KT, kThreads, kUnroll, kFast>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kExclusiveSmem));
     if (err != cudaSuccess) return err;
@@ -194,8 +249,10 @@ cudaError_t launch_shape(const CombineArgs& a, int num_sms, cudaStream_t stream)
 template <int KT>
 cudaError_t launch_k(const CombineArgs& a, int num_sms, cudaStream_t stream) {
     if (num_sms >= EP_COMBINE_WIDE_MIN_SMS)
-        return launch_shape<KT, EP_COMBINE_WIDE_THREADS, EP_COMBINE_WIDE_UNROLL>(a, num_sms, stream);
-    return launch_shape<KT, EP_COMBINE_NARROW_THREADS, EP_COMBINE_NARROW_UNROLL>(a, num_sms, stream);
+        return launch_shape<KT, EP_COMBINE_WIDE_THREADS, EP_COMBINE_WIDE_UNROLL, (KT > 0)>(
+            a, num_sms, stream);
+    return launch_shape<KT, EP_COMBINE_NARROW_THREADS, EP_COMBINE_NARROW_UNROLL,
+                        (KT > 0 && KT <= EP_COMBINE_NARROW_FAST_MAX_K)>(a, num_sms, stream);
 }
 
 }  // namespace
