@@ -19,8 +19,7 @@
 // writes 16 bytes, so every warp store is a coalesced 512-byte row segment.
 // Units whose K slots are all valid and which lie wholly inside the row take
 // an unpredicated body whose fmas go in packed fp32 pairs (fma.rn.f32x2,
-// the same rounding per element); the wide shape always has it, the narrow
-// one up to K = 6.
+// the same rounding per element), for every K <= 8.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -46,10 +45,10 @@ namespace {
 #ifndef EP_COMBINE_NARROW_UNROLL
 #define EP_COMBINE_NARROW_UNROLL 1
 #endif
-// The narrow shape takes the unpredicated fast path (below) only up to this
-// K: with more rows per unit its registers spill at 768 threads.
-#ifndef EP_COMBINE_NARROW_FAST_MAX_K
-#define EP_COMBINE_NARROW_FAST_MAX_K 6
+// The narrow shape for K = 7 and 8: fewer threads, so that the unpredicated
+// fast path (below) keeps its K row loads in registers without spilling.
+#ifndef EP_COMBINE_NARROW_THREADS_K8
+#define EP_COMBINE_NARROW_THREADS_K8 640
 #endif
 // Budgets of at least this many SMs use the wide shape.
 #ifndef EP_COMBINE_WIDE_MIN_SMS
@@ -251,8 +250,8 @@ cudaError_t launch_k(const CombineArgs& a, int num_sms, cudaStream_t stream) {
     if (num_sms >= EP_COMBINE_WIDE_MIN_SMS)
         return launch_shape<KT, EP_COMBINE_WIDE_THREADS, EP_COMBINE_WIDE_UNROLL, (KT > 0)>(
             a, num_sms, stream);
-    return launch_shape<KT, EP_COMBINE_NARROW_THREADS, EP_COMBINE_NARROW_UNROLL,
-                        (KT > 0 && KT <= EP_COMBINE_NARROW_FAST_MAX_K)>(a, num_sms, stream);
+    constexpr int kNarrow = KT >= 7 ? EP_COMBINE_NARROW_THREADS_K8 : EP_COMBINE_NARROW_THREADS;
+    return launch_shape<KT, kNarrow, EP_COMBINE_NARROW_UNROLL, (KT > 0)>(a, num_sms, stream);
 }
 
 }  // namespace
