@@ -32,24 +32,21 @@ namespace {
 
 // Two compiled shapes (threads per CTA, column blocks per unit), chosen by
 // the SM budget: with many SMs, fewer threads with two blocks in flight each
-// win; with few SMs, more threads (more loads in flight per SM) win.
+// win; with few SMs, as many threads as the registers allow (more loads in
+// flight per SM).
 #ifndef EP_COMBINE_WIDE_THREADS
 #define EP_COMBINE_WIDE_THREADS 384
 #endif
 #ifndef EP_COMBINE_WIDE_UNROLL
 #define EP_COMBINE_WIDE_UNROLL 2
 #endif
-#ifndef EP_COMBINE_NARROW_THREADS
-#define EP_COMBINE_NARROW_THREADS 768
-#endif
-#ifndef EP_COMBINE_NARROW_UNROLL
-#define EP_COMBINE_NARROW_UNROLL 1
-#endif
-// The narrow shape for K = 7 and 8: fewer threads, so that the unpredicated
-// fast path (below) keeps its K row loads in registers without spilling.
-#ifndef EP_COMBINE_NARROW_THREADS_K8
-#define EP_COMBINE_NARROW_THREADS_K8 640
-#endif
+// Narrow shape (one column block per unit): the most threads per CTA whose
+// register budget (65536 / threads) still holds the K row loads of the
+// unpredicated body without spilling; measured best at every budget of
+// 16-48 SMs for K = 2, 4, 5, 6 and 8. K > 8 (generic path): 768.
+constexpr int narrow_threads(int KT) {
+    return KT == 0 ? 768 : KT <= 5 ? 1024 : KT == 6 ? 896 : KT == 7 ? 768 : 640;
+}
 // Budgets of at least this many SMs use the wide shape.
 #ifndef EP_COMBINE_WIDE_MIN_SMS
 #define EP_COMBINE_WIDE_MIN_SMS 96
@@ -250,8 +247,7 @@ cudaError_t launch_k(const CombineArgs& a, int num_sms, cudaStream_t stream) {
     if (num_sms >= EP_COMBINE_WIDE_MIN_SMS)
         return launch_shape<KT, EP_COMBINE_WIDE_THREADS, EP_COMBINE_WIDE_UNROLL, (KT > 0)>(
             a, num_sms, stream);
-    constexpr int kNarrow = KT >= 7 ? EP_COMBINE_NARROW_THREADS_K8 : EP_COMBINE_NARROW_THREADS;
-    return launch_shape<KT, kNarrow, EP_COMBINE_NARROW_UNROLL, (KT > 0)>(a, num_sms, stream);
+    return launch_shape<KT, narrow_threads(KT), 1, (KT > 0)>(a, num_sms, stream);
 }
 
 }  // namespace
