@@ -19,7 +19,8 @@
 // writes 16 bytes, so every warp store is a coalesced 512-byte row segment.
 // Units whose K slots are all valid and which lie wholly inside the row take
 // an unpredicated body whose fmas go in packed fp32 pairs (fma.rn.f32x2,
-// the same rounding per element), for every K <= 8.
+// the same rounding per element), for every K <= 8. Below the wide budgets
+// each CTA runs as many threads as the registers allow (768 or 1024).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,13 +41,17 @@ namespace {
 #ifndef EP_COMBINE_WIDE_UNROLL
 #define EP_COMBINE_WIDE_UNROLL 2
 #endif
-// Narrow shape (one column block per unit): the most threads per CTA whose
-// register budget (65536 / threads) still holds the K row loads of the
-// unpredicated body without spilling; measured best at every budget of
-// 16-48 SMs for K = 2, 4, 5, 6 and 8. K > 8 (generic path): 768.
+// Narrow shape (one column block per unit): as many threads per CTA as the
+// register budget (65536 / threads) allows while the unpredicated body keeps
+// its K row loads in registers without spilling. For K >= 6 the rows are
+// addressed by 32-bit slot index instead of a 64-bit pointer per k (one more
+// multiply-add per load, 8-16 fewer registers), which buys the extra threads.
+// Measured best at 16-48 SMs for K = 2, 4, 5, 6 and 8. K > 8 (generic path):
+// 768.
 constexpr int narrow_threads(int KT) {
-    return KT == 0 ? 768 : KT <= 5 ? 1024 : KT == 6 ? 896 : KT == 7 ? 768 : 640;
+    return KT == 0 ? 768 : KT <= 6 ? 1024 : 768;
 }
+constexpr bool narrow_slot_rows(int KT) { return KT >= 6; }
 // Budgets of at least this many SMs use the wide shape.
 #ifndef EP_COMBINE_WIDE_MIN_SMS
 #define EP_COMBINE_WIDE_MIN_SMS 96
@@ -101,7 +106,7 @@ __device__ __forceinline__ uint4 round8(const float (&acc)[8]) {
 // registers). KT == 0: any K <= 32, broadcast per unit. A unit is UN
 // consecutive 512-byte column blocks of one token, so each lane keeps
 // UN * K independent 16-byte loads in flight.
-template <int KT, int kThreads, int kUnroll, bool kFast>
+template <int KT, int kThreads, int kUnroll, bool kFast, bool kSlotRows>
 __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs a) {
     griddep_wait();
     griddep_launch_dependents();
@@ -118,7 +123,12 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
     constexpr int KR = KT > 0 ? KT : 1;
 
     int64_t tok = -1;
-    const uint8_t* rowp[KR];
+    // expert row of each k (row 0 where masked): a slot index or a pointer
+    int32_t rowi[KR] = {};
+    const uint8_t* rowp[KR] = {};
+    auto row = [&](int k) -> const uint8_t* {
+        return kSlotRows ? a.expert_out + static_cast<int64_t>(rowi[k]) * a.row_bytes : rowp[k];
+    };
     float wk[KR];
     bool on[KR];
     bool all_on = false;  // every one of the token's K slots is valid (warp-uniform)
@@ -146,7 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
                     const int32_t sk = __shfl_sync(kFullMask, s, k);
                     wk[k] = __shfl_sync(kFullMask, w, k);
                     on[k] = sk >= 0;
-                    rowp[k] = a.expert_out + static_cast<int64_t>(sk < 0 ? 0 : sk) * a.row_bytes;
+                    if (kSlotRows)
+                        rowi[k] = sk < 0 ? 0 : sk;
+                    else
+                        rowp[k] = a.expert_out + static_cast<int64_t>(sk < 0 ? 0 : sk) * a.row_bytes;
                 }
                 all_on = __all_sync(kFullMask, lane >= K || s >= 0);
             }
@@ -159,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
 #pragma unroll
             for (int k = 0; k < KR; ++k)
 #pragma unroll
-                for (int j = 0; j < kUnroll; ++j) v[j][k] = ld_expert(rowp[k] + col0 + j * kColBytes);
+                for (int j = 0; j < kUnroll; ++j) v[j][k] = ld_expert(row(k) + col0 + j * kColBytes);
             float acc[kUnroll][8];
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
@@ -199,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
             for (int k = 0; k < KR; ++k)
 #pragma unroll
                 for (int j = 0; j < kUnroll; ++j)
-                    if (on[k] && in_row[j]) v[j][k] = ld_expert(rowp[k] + col0 + j * kColBytes);
+                    if (on[k] && in_row[j]) v[j][k] = ld_expert(row(k) + col0 + j * kColBytes);
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j)
 #pragma unroll
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
     }
 }
 
-template <int KT, int kThreads, int kUnroll, bool kFast>
+template <int KT, int kThreads, int kUnroll, bool kFast, bool kSlotRows>
 cudaError_t launch_shape(const CombineArgs& a, int num_sms, cudaStream_t stream) {
     constexpr uint32_t kUnitBytes = kColBytes * kUnroll;
     const int64_t units = a.T * ((a.row_bytes + kUnitBytes - 1) / kUnitBytes);
@@ -235,7 +248,7 @@ cudaError_t launch_shape(const CombineArgs& a, int num_sms, cudaStream_t stream)
     const int64_t ctas_needed = (units + warps_per_cta - 1) / warps_per_cta;
     const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
     if (grid <= 0) return cudaSuccess;
-    auto kern = combine_kernel<KT, kThreads, kUnroll, kFast>;
+    auto kern = combine_kernel<KT, kThreads, kUnroll, kFast, kSlotRows>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kExclusiveSmem));
     if (err != cudaSuccess) return err;
@@ -245,9 +258,10 @@ cudaError_t launch_shape(const CombineArgs& a, int num_sms, cudaStream_t stream)
 template <int KT>
 cudaError_t launch_k(const CombineArgs& a, int num_sms, cudaStream_t stream) {
     if (num_sms >= EP_COMBINE_WIDE_MIN_SMS)
-        return launch_shape<KT, EP_COMBINE_WIDE_THREADS, EP_COMBINE_WIDE_UNROLL, (KT > 0)>(
+        return launch_shape<KT, EP_COMBINE_WIDE_THREADS, EP_COMBINE_WIDE_UNROLL, (KT > 0), false>(
             a, num_sms, stream);
-    return launch_shape<KT, narrow_threads(KT), 1, (KT > 0)>(a, num_sms, stream);
+    return launch_shape<KT, narrow_threads(KT), 1, (KT > 0), narrow_slot_rows(KT)>(a, num_sms,
+                                                                                  stream);
 }
 
 }  // namespace
