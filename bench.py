@@ -1044,6 +1044,11 @@ def main():
                 "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                # host-link bytes moved per second over both directions: the
+                # e2e step is bound by the CPU-GPU link (~300 GB/s with both
+                # directions busy on GB300, copy engines or SMs alike)
+                "host_link_gbs": (e2e["h2d_bytes_per_step"] + e2e["d2h_bytes_per_step"])
+                                 / (e2e_ms * 1e-3) / 1e9,
             },
             "gpu_launches": step.launches_per_step * args.steps,
             "clocks": main_run["clocks"],
