@@ -621,6 +621,9 @@ extern "C" {
 int bw_write(void* p, size_t n, int grid, int block) { k_write<<<grid, block>>>((uint4*)p, n / 16); return cudaGetLastError(); }
 int bw_read(void* p, size_t n, void* sink, int grid, int block) { k_read<<<grid, block>>>((const uint4*)p, n / 16, (uint32_t*)sink); return cudaGetLastError(); }
 int bw_copy(void* a, void* b, size_t n, int grid, int block) { k_copy<<<grid, block>>>((const uint4*)a, (uint4*)b, n / 16); return cudaGetLastError(); }
+int bw_copy_on(void* a, void* b, size_t n, int grid, int block, void* stream) {
+    k_copy<<<grid, block, 0, (cudaStream_t)stream>>>((const uint4*)a, (uint4*)b, n / 16); return cudaGetLastError(); }
+int host_dev_ptr(void* host, void** dev) { return cudaHostGetDevicePointer(dev, host, 0); }
 int bw_bulk_write(void* p, size_t n, int grid, int warps) {
     cudaFuncSetAttribute(k_bulk_write, cudaFuncAttributeMaxDynamicSharedMemorySize, warps * 8192);
     k_bulk_write<<<grid, warps * 32, warps * 8192>>>((uint8_t*)p, n); return cudaGetLastError(); }
@@ -716,7 +719,9 @@ def run_pipeline_model(ep, dev, wl: W.Workload, budgets=(0, 24, 16)) -> None:
 def measure_ceilings(dev) -> dict:
     """Write-only, read-only and copy bandwidth of plain streaming kernels
     (16-byte vectors; 8 KB bulk stores), all SMs and 24 SMs, plus pinned
-    host<->device copy rates. Built from the source above with nvcc."""
+    host<->device rates: copy engines one way and both ways at once, and the
+    copy kernel reading or writing the pinned buffers directly (zero-copy).
+    Built from the source above with nvcc."""
     import ctypes
     L = _probe_lib()
     vp, sz = ctypes.c_void_p, ctypes.c_size_t
@@ -748,9 +753,44 @@ def measure_ceilings(dev) -> dict:
     r["bulk_write_sms_24"] = best(lambda: L.bw_bulk_write(vp(a.data_ptr()), sz(n), 24, 24), n)
     m = 59 * 1024 * 1024
     h = torch.ones(m, dtype=torch.uint8).pin_memory()
+    h2 = torch.empty(m, dtype=torch.uint8).pin_memory()
     d = torch.empty(m, dtype=torch.uint8, device=dev)
+    d2 = torch.ones(m, dtype=torch.uint8, device=dev)
     r["h2d_gbs"] = best(lambda: (d.copy_(h, non_blocking=True), 0)[1], m)
     r["d2h_gbs"] = best(lambda: (h.copy_(d, non_blocking=True), 0)[1], m)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def both(f1, f2):
+        ev = torch.cuda.Event()
+        ev.record()
+        s1.wait_event(ev)
+        s2.wait_event(ev)
+        f1(s1)
+        f2(s2)
+        for s_ in (s1, s2):
+            e_ = torch.cuda.Event()
+            e_.record(s_)
+            torch.cuda.current_stream().wait_event(e_)
+        return 0
+
+    def ce(dst, src):
+        def f(s_):
+            with torch.cuda.stream(s_):
+                dst.copy_(src, non_blocking=True)
+        return f
+    r["h2d_d2h_concurrent_gbs"] = best(lambda: both(ce(d, h), ce(h2, d2)), 2 * m)
+    # SM-driven zero-copy: the copy kernel loads from / stores to the pinned
+    # buffers through their device pointers (16-byte vectors)
+    hp, hp2 = ctypes.c_void_p(), ctypes.c_void_p()
+    if L.host_dev_ptr(vp(h.data_ptr()), ctypes.byref(hp)) == 0 and \
+            L.host_dev_ptr(vp(h2.data_ptr()), ctypes.byref(hp2)) == 0:
+        def sm(src, dst, g):
+            return lambda s_: L.bw_copy_on(src, dst, sz(m), g, 1024, vp(s_.cuda_stream))
+        for g in (16, 152):
+            r[f"sm_h2d_gbs_{g}"] = best(lambda: L.bw_copy(hp, vp(d.data_ptr()), sz(m), g, 1024), m)
+            r[f"sm_d2h_gbs_{g}"] = best(lambda: L.bw_copy(vp(d2.data_ptr()), hp2, sz(m), g, 1024), m)
+        r["sm_h2d_d2h_concurrent_gbs"] = best(
+            lambda: both(sm(hp, vp(d.data_ptr()), 32), sm(vp(d2.data_ptr()), hp2, 32)), 2 * m)
     return r
 
 
