@@ -190,6 +190,9 @@ def _custom(T, H, E, K, seed=7, mask=0.0, routing="uniform"):
     (9000, 64, 256, 1, 0.0),    # K = 1, multi-tile layout
     (20000, 16, 4096, 8, 0.05), # more tiles than one launch holds: tile + finish kernels
     (70000, 8, 4096, 8, 0.0),   # over 512 tiles: separate one-block scan
+    (300, 2048, 16, 5, 0.0),    # K = 5: combine at 1024 threads, row pointers
+    (257, 1000, 32, 7, 0.05),   # K = 7: rows by slot index; masked and partial-row units
+    (129, 4104, 64, 6, 0.0),    # K = 6: rows by slot index, last unit partial
 ])
 def test_edge_shapes(ep, T, H, E, K, mask):
     inp = _custom(T, H, E, K, mask=mask)
