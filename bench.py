@@ -228,11 +228,15 @@ def max_over_ranks(v: float, dist_on: bool) -> float:
 def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch.cuda.Stream,
                sampler_index: int = -1) -> dict:
     """W untimed steps, then exactly K steps between barrier+synchronize,
-    with per-kernel CUDA events recorded on the launching stream."""
+    timed by CUDA events on the launching stream around the whole loop (the
+    headline: nothing between the kernels, so each may start while the
+    previous one finishes). Then K more steps with an event between every
+    two kernels for the per-kernel breakdown; those events stop the kernels
+    from overlapping, so that pass can be a little slower at small budgets
+    (its total is reported as total_ms_kernel_events)."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             step.run(step.b, stream)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
@@ -241,6 +245,20 @@ def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch
         if sampler:
             sampler.__enter__()
         start.record(stream)
+        for _ in range(steps):
+            step.run(step.b, stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.__exit__(None, None, None)
+        barrier(dist_on)
+        total_ms = start.elapsed_time(end)
+
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        start2 = torch.cuda.Event(enable_timing=True)
+        end2 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start2.record(stream)
         for i in range(steps):
             e = ev[i]
             e[0].record(stream)
@@ -250,31 +268,35 @@ def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch
             e[2].record(stream)
             step.combine(step.b, stream)
             e[3].record(stream)
-        end.record(stream)
+        end2.record(stream)
         torch.cuda.synchronize()
-        if sampler:
-            sampler.__exit__(None, None, None)
-        barrier(dist_on)
-    total_ms = start.elapsed_time(end)
     lay = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
     dis = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
     com = [ev[i][2].elapsed_time(ev[i][3]) for i in range(steps)]
-    return {"total_ms": total_ms, "layout_ms": lay, "dispatch_ms": dis, "combine_ms": com,
+    return {"total_ms": total_ms, "total_ms_kernel_events": start2.elapsed_time(end2),
+            "layout_ms": lay, "dispatch_ms": dis, "combine_ms": com,
             "clocks": sampler.summary() if sampler else None}
 
 
 def time_fused_steps(step: Step, steps: int, warmup: int, dist_on: bool,
                      stream: torch.cuda.Stream) -> dict:
-    """The same step with layout and dispatch in one call (ep_layout_dispatch)."""
+    """The same step with layout and dispatch in one call (ep_layout_dispatch);
+    total without events between the kernels, then a pass with them for the
+    per-kernel breakdown (as in time_steps)."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             step.run_fused(step.b, stream)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         barrier(dist_on)
         start.record(stream)
+        for _ in range(steps):
+            step.run_fused(step.b, stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist_on)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
         for i in range(steps):
             e = ev[i]
             e[0].record(stream)
@@ -282,9 +304,7 @@ def time_fused_steps(step: Step, steps: int, warmup: int, dist_on: bool,
             e[1].record(stream)
             step.combine(step.b, stream)
             e[2].record(stream)
-        end.record(stream)
         torch.cuda.synchronize()
-        barrier(dist_on)
     return {"total_ms": start.elapsed_time(end),
             "layout_dispatch_ms": [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)],
             "combine_ms": [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]}
@@ -1015,6 +1035,7 @@ def main():
         moved = ab["dispatch"] + ab["combine"]
         return {
             "num_sms": nsms, "ms_per_step": ms,
+            "ms_per_step_kernel_events": run["total_ms_kernel_events"] / args.steps,
             "tokens_per_s": world * step.T / (ms * 1e-3),
             "dispatch_combine_gbs": moved / ((d + c) * 1e-3) / 1e9,
             "dispatch_combine_frac": moved / ((d + c) * 1e-3) / 1e9 / peak,

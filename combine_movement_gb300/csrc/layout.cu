@@ -678,13 +678,16 @@ cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,
         cfg.blockDim = dim3(static_cast<unsigned>(threads));
         cfg.dynamicSmemBytes = p.smem;
         cfg.stream = stream;
-        cudaLaunchAttribute attr{};
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = static_cast<unsigned>(p.num_tiles);
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
+        cudaLaunchAttribute attr[2]{};
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.num_tiles);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        // as launch_dependent: may start while the previous kernel finishes
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = EP_PDL ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
         return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, idx, N, E, p.rounds, counts, offsets,
                                   slot, status);
     }
