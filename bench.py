@@ -479,11 +479,38 @@ def decode_latency(ep, dev, budgets=(16, 24, 0)) -> dict:
         cold = time_call(lambda: step.run(step.b), 30, flush)
         fwarm = time_call(lambda: step.run_fused(step.b), 200)
         fcold = time_call(lambda: step.run_fused(step.b), 30, flush)
+        # the same three calls captured once into a CUDA graph and replayed
+        # (one host launch per step)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step.run(step.b, torch.cuda.current_stream())
+        gwarm = time_call(g.replay, 200)
+
+        def back_to_back(fn, n=500):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / n * 1e3
+        out_b2b = back_to_back(lambda: step.run(step.b))
+        graph_b2b = back_to_back(g.replay)
         out[f"sms_{b or 'all'}"] = {
             "warm_us": round(warm, 2), "cold_us": round(cold, 2),
             "cold_gbs": round((ab["dispatch"] + ab["combine"]) / (cold * 1e-6) / 1e9, 1),
             "fused_warm_us": round(fwarm, 2), "fused_cold_us": round(fcold, 2),
+            "graph_warm_us": round(gwarm, 2),
+            # steps issued back to back from the host (no spin in between):
+            # the eager calls are bound by the host's launch rate, the graph
+            # is not
+            "back_to_back_us": round(out_b2b, 2), "graph_back_to_back_us": round(graph_b2b, 2),
         }
+        del g
     ep.ep_set_num_sms(0)
     return out
 

@@ -345,6 +345,63 @@ def test_back_to_back_batches_share_buffers_on_one_stream(ep):
     ep.ep_set_num_sms(0)
 
 
+@pytest.mark.parametrize("T,H,E,K", [
+    (128, 7168, 256, 8),   # decode: one-block layout
+    (2048, 2048, 64, 8),   # one thread-block cluster layout
+    (16384, 64, 128, 8),   # cooperative layout (grid barrier, generation word)
+])
+def test_cuda_graph_capture_and_replay(ep, T, H, E, K):
+    """The three calls captured once into a CUDA graph (with the expert
+    stand-in between them) and replayed on new inputs copied into the same
+    buffers: every entry point only enqueues launches, so the graph replays
+    the whole step; each replay is compared with the oracle."""
+    dev = torch.device("cuda:0")
+    inps = [_custom(T, H, E, K, seed=20 + i) for i in range(3)]
+    refs = [oracle_path(inp, T * K, 1.5) for inp in inps]
+    idx = inps[0].topk_idx.to(dev).clone()
+    w = inps[0].topk_w.to(dev).clone()
+    x = inps[0].x.to(dev).clone()
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    nws = ep.ep_layout_workspace_bytes(T, K, E)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev) if nws else None
+    recv = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+    eo = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ep.ep_set_num_sms(24)
+
+    def step(stream):
+        ep.ep_get_dispatch_layout(idx, E, counts, offsets, slot, ws, status, stream)
+        ep.ep_dispatch(x, slot, recv, None, None, None, status, stream)
+        eo.copy_(W.expert_standin(recv, 1.5))
+        ep.ep_combine(eo, slot, w, y, status, stream)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step(s)  # eager warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(torch.cuda.current_stream())
+    try:
+        for inp, ref in zip(inps, refs):
+            idx.copy_(inp.topk_idx)
+            w.copy_(inp.topk_w)
+            x.copy_(inp.x)
+            slot.fill_(-9)
+            y.fill_(0)
+            g.replay()
+            torch.cuda.synchronize()
+            assert ep.ep_get_status(status) == ep.EP_OK
+            assert np.array_equal(slot.cpu().numpy(), ref.slot)
+            assert np.array_equal(offsets.cpu().numpy(), ref.offsets)
+            assert np.array_equal(bits(y), ref.y)
+    finally:
+        ep.ep_set_num_sms(0)
+
+
 # ---- ep_layout_dispatch: layout and dispatch in one launch -----------------
 
 @pytest.mark.parametrize("name,budgets", [
