@@ -391,6 +391,7 @@ def cpu_baseline(inp: W.Inputs, budget_s: float = 10.0) -> dict:
         spent += oracle_sample(inp, tokens)
         done += 1
     return {"value": tokens * done / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "host_cores": os.cpu_count(),
             "sample": f"first {tokens} tokens of {inp.wl.name} (layout+dispatch+combine, "
                       f"identity experts), {done} repetitions, {spent:.1f} s single-threaded"}
 
