@@ -47,15 +47,22 @@ def is_stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and not is_stale():
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          out_dir: str | None = None) -> str:
+    """Build the library; returns its path. With ``out_dir`` the objects and
+    the library go there instead of in-tree (used to build the measured
+    alternatives, e.g. ``extra_flags=["-DEP_COMBINE_MODE=1"]``, beside the
+    default library)."""
+    lib_path = os.path.join(out_dir, "libep_gb300.so") if out_dir else LIB_PATH
+    obj_dir = os.path.join(out_dir, "_objs") if out_dir else OBJ_DIR
+    if out_dir is None and not force and not is_stale():
         return LIB_PATH
     nvcc = _nvcc()
-    os.makedirs(OBJ_DIR, exist_ok=True)
+    os.makedirs(obj_dir, exist_ok=True)
     flags = NVCC_FLAGS + list(extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ_DIR, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, os.path.basename(src).replace(".cu", ".o"))
         cmd = [nvcc, *flags, "-I", INCLUDE, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,13 +74,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, "-shared", f"-gencode={GENCODE}", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
