@@ -59,6 +59,21 @@ int sms_in_effect(int sm_count) {
     return (b <= 0 || b > sm_count) ? sm_count : b;
 }
 
+}  // namespace
+
+namespace ep {
+// Programmatic dependent launch only while the SM budget covers the whole
+// current device (see launch_dependent).
+bool launch_overlap_allowed() {
+    if (!EP_PDL) return false;
+    int c = 0, s = 0;
+    if (!device_limits(&c, &s)) return false;
+    return sms_in_effect(c) == c;
+}
+}  // namespace ep
+
+namespace {
+
 ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 
 // Which combine kernel runs: the direct 16-byte gather (0), the bulk-copy

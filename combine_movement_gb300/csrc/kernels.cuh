@@ -99,16 +99,22 @@ bool combine_tma_supported(int K);
 cudaError_t launch_combine_tma(const CombineArgs& a, int num_sms, int smem_optin,
                                cudaStream_t stream);
 
-// Launch a kernel of the hot path. With EP_PDL=1 (the default) the launch
-// allows it to start while the previous kernel on the stream finishes
-// (programmatic dependent launch): its CTAs become resident and wait in
-// griddep_wait(), which every such kernel calls before touching global
-// memory, so the launch latency overlaps the previous kernel's tail. On the
-// decode step (T=128) this saves 3-5 us of ~21-41 us; on the DeepSeek-V3
-// prefill step it makes no measurable difference.
+// Launch a kernel of the hot path. With programmatic dependent launch the
+// launch may start while the previous kernel on the stream finishes: its CTAs
+// become resident and wait in griddep_wait(), which every such kernel calls
+// before touching global memory, so the launch latency overlaps the previous
+// kernel's tail. On the DeepSeek-V3 prefill step this saves ~2 us of ~193;
+// on the decode step (T=128) 3-5 us of ~21-41.
+// It is used only while the SM budget covers the whole GPU
+// (launch_overlap_allowed()). A smaller budget means the GPU is shared with
+// concurrent work, and there the early launches measured slower: dispatch +
+// combine on 24 SMs next to an ALU-bound kernel on the other 128 took 24 %
+// longer with them than without, and 0 % longer without them.
 #ifndef EP_PDL
 #define EP_PDL 1
 #endif
+bool launch_overlap_allowed();
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent(void (*kernel)(KArgs...), int grid, int block, size_t smem,
                              cudaStream_t stream, Args&&... args) {
@@ -119,7 +125,7 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), int grid, int block, size
     cfg.stream = stream;
     cudaLaunchAttribute attr{};
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = EP_PDL ? 1 : 0;
+    attr.val.programmaticStreamSerializationAllowed = launch_overlap_allowed() ? 1 : 0;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);

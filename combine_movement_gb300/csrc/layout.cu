@@ -11,7 +11,7 @@
 // Entries are the T*K routing-table cells in row-major order (i = t*K + k).
 // The table is cut into tiles of `warps * 32 * rounds` entries:
 //   1. tile kernel (one block per tile): loads the tile's ids once, counts
-//      them per warp (warp match), scans across warps and assigns every entry
+//      them per warp (ballot peer groups), scans across warps and assigns every entry
 //      its rank among the tile's entries of the same expert, in entry order;
 //      writes the tile's per-expert counts to tile_counts[tile][e] and the
 //      packed (rank, expert) into slot.
@@ -83,8 +83,8 @@ __device__ __forceinline__ void scan_across_warps(int32_t* run, int E, int nwarp
 // ---- tile kernel: per-warp counts, per-tile ranks ----------------------------
 // Every warp owns `rounds` consecutive 32-entry rounds of its tile; all of
 // its routing ids are loaded up front (one memory latency, not one per
-// round). Pass A counts ids per warp (warp match: one shared-memory add per
-// distinct id per round); a scan across the warps turns the counts into
+// round). Pass A counts ids per warp (ballot peer groups: one shared-memory
+// add per distinct id per round); a scan across the warps turns the counts into
 // per-warp starting ranks; pass B hands out ranks in entry order.
 //  FUSED (the whole table is one tile): the block also scans across experts
 //    and writes counts, offsets and final slots.
@@ -685,7 +685,7 @@ cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,
         attr[0].val.clusterDim.z = 1;
         // as launch_dependent: may start while the previous kernel finishes
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[1].val.programmaticStreamSerializationAllowed = EP_PDL ? 1 : 0;
+        attr[1].val.programmaticStreamSerializationAllowed = launch_overlap_allowed() ? 1 : 0;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, idx, N, E, p.rounds, counts, offsets,
