@@ -204,6 +204,36 @@ def test_edge_shapes(ep, T, H, E, K, mask):
         assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=b), ref)
 
 
+def _fuzz_cases(n=24, seed=2024):
+    """Seeded random shapes: T, H (a multiple of 8), E, K <= min(E, 32),
+    masking, routing and SM budget drawn at random, sized so the oracle
+    finishes each in well under a second."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        E = int(rng.choice([1, 2, 3, 7, 16, 33, 64, 128, 256, 300, 1024, 4096]))
+        K = int(rng.integers(1, min(E, 32) + 1))
+        T = int(rng.integers(1, 3000))
+        H = 8 * int(rng.integers(1, 1200))
+        while T * H > 4_000_000:
+            H = max(8, H // 2 // 8 * 8)
+            T = max(1, T // 2)
+        mask = float(rng.choice([0.0, 0.0, 0.05, 0.5]))
+        routing = "zipf" if (rng.random() < 0.3 and K < E) else "uniform"
+        budget = int(rng.choice([0, 0, 1, 2, 5, 24, 100]))
+        cases.append((T, H, E, K, mask, routing, budget, 100 + i))
+    return cases
+
+
+@pytest.mark.parametrize("T,H,E,K,mask,routing,budget,seed", _fuzz_cases())
+def test_random_shapes(ep, T, H, E, K, mask, routing, budget, seed):
+    inp = _custom(T, H, E, K, seed=seed, mask=mask, routing=routing)
+    R_valid = int((inp.topk_idx >= 0).sum())
+    num_recv = R_valid + 1
+    ref = oracle_path(inp, num_recv, 1.5)
+    assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget), ref)
+
+
 def test_empty_batch(ep):
     inp = _custom(0, 64, 8, 2)
     ref = oracle_path(inp, 0, 1.0)
