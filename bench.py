@@ -1128,6 +1128,15 @@ def main():
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_bytes": ab[dom],
             },
+            # the same figures for both HBM-bound kernels (all SMs and the
+            # second budget); the layout is latency-bound and has none
+            "roofline_by_kernel": {
+                f"{k}_{tag}": {"achieved": r[f"{k}_gbs"], "frac": r[f"{k}_gbs"] / peak,
+                               "us": r[f"{k}_us"], "algorithmic_bytes": ab[k],
+                               "traffic": kernel_traffic(k) if tag == "all_sms" else None}
+                for k in ("dispatch", "combine")
+                for tag, r in (("all_sms", s_all), (f"sms_{args.budget_sms}", s_bud))
+            },
             "e2e": {
                 "value": world * step.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "ms_per_step": e2e_ms,
