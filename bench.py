@@ -893,8 +893,9 @@ def run_overlap(ep, dev, budgets=(16, 24, 48), steps: int = 60) -> None:
             step.dispatch(step.b, s_move)
             step.combine(step.b, s_move)
 
-    for n in budgets:
+    for n, mode in [(n, m) for n in budgets for m in (0, 1)]:
         ep.ep_set_num_sms(n)
+        ep.ep_set_launch_overlap(mode)  # 0: library default (no overlap below the full budget)
         grid = sms - n
         with torch.cuda.stream(s_move):
             movement(3)
@@ -933,6 +934,7 @@ def run_overlap(ep, dev, budgets=(16, 24, 48), steps: int = 60) -> None:
         flops = 4 * 2 * iters * 1024 * grid
         print(json.dumps({
             "num_sms_movement": n, "num_sms_alu": grid, "steps": steps,
+            "launch_overlap": "auto (off below the full budget)" if mode == 0 else "forced on",
             "movement_ms_per_step_alone": round(move_ms / steps, 4),
             "movement_ms_per_step_overlapped": round(a0.elapsed_time(a1) / steps, 4),
             "alu_ms_alone": round(comp_ms, 3), "alu_ms_overlapped": round(c0.elapsed_time(c1), 3),
@@ -941,6 +943,7 @@ def run_overlap(ep, dev, budgets=(16, 24, 48), steps: int = 60) -> None:
             "clocks_overlapped": sampler.summary(),
         }), flush=True)
     ep.ep_set_num_sms(0)
+    ep.ep_set_launch_overlap(0)
 
 
 # ---------------------------------------------------------------------------

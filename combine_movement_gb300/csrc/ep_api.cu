@@ -21,6 +21,7 @@
 namespace {
 
 std::atomic<int> g_num_sms{0};
+std::atomic<int> g_overlap_mode{0};  // 0 auto, 1 always, 2 never
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -66,6 +67,9 @@ namespace ep {
 // current device (see launch_dependent).
 bool launch_overlap_allowed() {
     if (!EP_PDL) return false;
+    const int mode = g_overlap_mode.load(std::memory_order_relaxed);
+    if (mode == 1) return true;
+    if (mode == 2) return false;
     int c = 0, s = 0;
     if (!device_limits(&c, &s)) return false;
     return sms_in_effect(c) == c;
@@ -159,6 +163,14 @@ int ep_set_num_sms(int num_sms) {
 }
 
 int ep_get_num_sms(void) { return g_num_sms.load(std::memory_order_relaxed); }
+
+int ep_set_launch_overlap(int mode) {
+    if (mode < 0 || mode > 2) return -1;
+    g_overlap_mode.store(mode, std::memory_order_relaxed);
+    return mode;
+}
+
+int ep_get_launch_overlap(void) { return g_overlap_mode.load(std::memory_order_relaxed); }
 
 int ep_num_sms_in_effect(void) {
     int c = 0, s = 0;

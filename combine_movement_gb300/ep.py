@@ -49,6 +49,10 @@ def _load() -> ctypes.CDLL:
     lib.ep_set_num_sms.restype = i32
     lib.ep_get_num_sms.argtypes = []
     lib.ep_get_num_sms.restype = i32
+    lib.ep_set_launch_overlap.argtypes = [i32]
+    lib.ep_set_launch_overlap.restype = i32
+    lib.ep_get_launch_overlap.argtypes = []
+    lib.ep_get_launch_overlap.restype = i32
     lib.ep_num_sms_in_effect.argtypes = []
     lib.ep_num_sms_in_effect.restype = i32
     lib.ep_layout_workspace_bytes.argtypes = [i64, i32, i32]
@@ -116,6 +120,14 @@ def ep_set_num_sms(num_sms: int) -> int:
 
 def ep_get_num_sms() -> int:
     return lib.ep_get_num_sms()
+
+
+def ep_set_launch_overlap(mode: int) -> int:
+    return lib.ep_set_launch_overlap(mode)
+
+
+def ep_get_launch_overlap() -> int:
+    return lib.ep_get_launch_overlap()
 
 
 def ep_num_sms_in_effect() -> int:

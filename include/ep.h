@@ -99,6 +99,18 @@ EP_API int ep_set_num_sms(int num_sms);
 /* The stored SM budget (0 = all). */
 EP_API int ep_get_num_sms(void);
 
+/* Whether a kernel launch may overlap the tail of the previous kernel on the
+ * stream (programmatic dependent launch; each kernel still waits for its
+ * predecessor's results before touching global memory):
+ *   0  auto (default): only while the SM budget covers the whole GPU. A
+ *      smaller budget usually means the GPU is shared with concurrent work,
+ *      and there the early launches slowed dispatch + combine measurably.
+ *   1  always;  2  never.
+ * Process-wide, like the SM budget. Returns the stored mode, or -1 (and
+ * changes nothing) for any other value. */
+EP_API int ep_set_launch_overlap(int mode);
+EP_API int ep_get_launch_overlap(void);
+
 /* The number of SMs dispatch/combine will use on the current device: the
  * budget clamped to [1, SM count]. Returns -1 if the device can't be queried. */
 EP_API int ep_num_sms_in_effect(void);

@@ -56,6 +56,19 @@ def test_sm_budget_is_stored(ep):
         ep.ep_set_num_sms(old)
 
 
+def test_launch_overlap_mode_is_stored(ep):
+    try:
+        assert ep.ep_get_launch_overlap() == 0          # auto by default
+        assert ep.ep_set_launch_overlap(1) == 1
+        assert ep.ep_get_launch_overlap() == 1
+        assert ep.ep_set_launch_overlap(3) == -1        # invalid: unchanged
+        assert ep.ep_set_launch_overlap(-1) == -1
+        assert ep.ep_get_launch_overlap() == 1
+        assert ep.ep_set_launch_overlap(2) == 2
+    finally:
+        ep.ep_set_launch_overlap(0)
+
+
 def test_status_strings(ep):
     for code in range(8):
         s = ep.ep_status_string(code)

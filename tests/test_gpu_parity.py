@@ -353,8 +353,11 @@ def test_back_to_back_batches_share_buffers_on_one_stream(ep):
                 y=torch.empty((T, H), dtype=torch.bfloat16).pin_memory()) for _ in cases]
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
-    for b in (0, 24):
+    # budgets with the default launch policy, and 24 SMs with overlapping
+    # launches forced on
+    for b, mode in ((0, 0), (24, 0), (24, 1)):
         ep.ep_set_num_sms(b)
+        ep.ep_set_launch_overlap(mode)
         with torch.cuda.stream(s):
             for i, (_, _, _, sc) in enumerate(cases):
                 ep.ep_get_dispatch_layout(idx[i], E, counts, offsets, slot, ws, status, s)
@@ -373,6 +376,7 @@ def test_back_to_back_batches_share_buffers_on_one_stream(ep):
             assert np.array_equal(r[:valid], ref.recv_x[:valid]), f"batch {i}: recv_x"
             assert np.array_equal(bits(out[i]["y"]), ref.y), f"batch {i}: y"
     ep.ep_set_num_sms(0)
+    ep.ep_set_launch_overlap(0)
 
 
 @pytest.mark.parametrize("T,H,E,K", [
