@@ -594,12 +594,12 @@ __global__ void k_bulk_write(uint8_t* dst, size_t nbytes) {
     }
 }
 // Stage probes for the two-stage pipeline model of the dispatch ring: the
-// same per-warp ring shape (4 stages, 2 loads ahead, one elected lane, the
+// same per-warp ring shape (3 or 4 stages, 2 loads ahead, one elected lane, the
 // same chunk and units per warp) doing only its load stage or only its store
 // stage, over buffers of their own. Every mbarrier wait gives up after 2 s
 // and records it in *err; after a give-up the lane still waits (bounded) for
 // the loads it issued, so no copy lands in shared memory after the CTA ends.
-constexpr int kNS = 4, kP = 2;
+constexpr int kP = 2;
 __device__ __forceinline__ bool probe_wait(uint32_t bar, uint32_t parity) {
     uint64_t t0;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
@@ -613,14 +613,16 @@ __device__ __forceinline__ bool probe_wait(uint32_t bar, uint32_t parity) {
         if (t - t0 > 2000000000ull) return false;
     }
 }
+template <int kNS>
 __host__ __device__ constexpr uint32_t ring_region(int warps) { return (8u * kNS * warps + 127u) & ~127u; }
+template <int kNS>
 __global__ void k_ring_load(const uint8_t* src, long long units, uint32_t chunk, int* err) {
     extern __shared__ __align__(128) uint8_t sm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
     if (lane != 0) return;
     const uint32_t base = (uint32_t)__cvta_generic_to_shared(sm);
     const uint32_t bar0 = base + 8u * kNS * warp;
-    const uint32_t buf0 = base + ring_region(nw) + kNS * chunk * warp;
+    const uint32_t buf0 = base + ring_region<kNS>(nw) + kNS * chunk * warp;
     for (int s = 0; s < kNS; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar0 + 8u * s) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     const long long W = (long long)gridDim.x * nw, gw = (long long)blockIdx.x * nw + warp;
@@ -644,10 +646,11 @@ __global__ void k_ring_load(const uint8_t* src, long long units, uint32_t chunk,
         }
     }
 }
+template <int kNS>
 __global__ void k_ring_store(uint8_t* dst, long long units, uint32_t chunk, int K) {
     extern __shared__ __align__(128) uint8_t sm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
-    uint8_t* mine = sm + ring_region(nw) + (size_t)kNS * chunk * warp;
+    uint8_t* mine = sm + ring_region<kNS>(nw) + (size_t)kNS * chunk * warp;
     for (uint32_t i = lane; i < kNS * chunk / 4; i += 32) reinterpret_cast<uint32_t*>(mine)[i] = i;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
@@ -665,6 +668,18 @@ __global__ void k_ring_store(uint8_t* dst, long long units, uint32_t chunk, int 
     }
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+template <int kNS>
+int ring_load_ns(const void* src, long long units, unsigned chunk, int grid, int warps, int* err) {
+    const int smem = (int)(ring_region<kNS>(warps) + (size_t)kNS * chunk * warps);
+    cudaError_t e = cudaFuncSetAttribute(k_ring_load<kNS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k_ring_load<kNS><<<grid, warps * 32, smem>>>((const uint8_t*)src, units, chunk, err); return cudaGetLastError(); }
+template <int kNS>
+int ring_store_ns(void* dst, long long units, unsigned chunk, int K, int grid, int warps) {
+    const int smem = (int)(ring_region<kNS>(warps) + (size_t)kNS * chunk * warps);
+    cudaError_t e = cudaFuncSetAttribute(k_ring_store<kNS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k_ring_store<kNS><<<grid, warps * 32, smem>>>((uint8_t*)dst, units, chunk, K); return cudaGetLastError(); }
 extern "C" {
 int bw_write(void* p, size_t n, int grid, int block) { k_write<<<grid, block>>>((uint4*)p, n / 16); return cudaGetLastError(); }
 int bw_read(void* p, size_t n, void* sink, int grid, int block) { k_read<<<grid, block>>>((const uint4*)p, n / 16, (uint32_t*)sink); return cudaGetLastError(); }
@@ -675,17 +690,12 @@ int host_dev_ptr(void* host, void** dev) { return cudaHostGetDevicePointer(dev, 
 int bw_bulk_write(void* p, size_t n, int grid, int warps) {
     cudaFuncSetAttribute(k_bulk_write, cudaFuncAttributeMaxDynamicSharedMemorySize, warps * 8192);
     k_bulk_write<<<grid, warps * 32, warps * 8192>>>((uint8_t*)p, n); return cudaGetLastError(); }
-int ring_smem(int warps, unsigned chunk) { return (int)(ring_region(warps) + (size_t)kNS * chunk * warps); }
-int ring_load(const void* src, long long units, unsigned chunk, int grid, int warps, int* err) {
-    const int smem = ring_smem(warps, chunk);
-    cudaError_t e = cudaFuncSetAttribute(k_ring_load, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    k_ring_load<<<grid, warps * 32, smem>>>((const uint8_t*)src, units, chunk, err); return cudaGetLastError(); }
-int ring_store(void* dst, long long units, unsigned chunk, int K, int grid, int warps) {
-    const int smem = ring_smem(warps, chunk);
-    cudaError_t e = cudaFuncSetAttribute(k_ring_store, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    k_ring_store<<<grid, warps * 32, smem>>>((uint8_t*)dst, units, chunk, K); return cudaGetLastError(); }
+int ring_load(const void* src, long long units, unsigned chunk, int grid, int warps, int stages, int* err) {
+    return stages == 3 ? ring_load_ns<3>(src, units, chunk, grid, warps, err)
+                       : ring_load_ns<4>(src, units, chunk, grid, warps, err); }
+int ring_store(void* dst, long long units, unsigned chunk, int K, int grid, int warps, int stages) {
+    return stages == 3 ? ring_store_ns<3>(dst, units, chunk, K, grid, warps)
+                       : ring_store_ns<4>(dst, units, chunk, K, grid, warps); }
 }
 """
 
@@ -738,12 +748,15 @@ def run_pipeline_model(ep, dev, wl: W.Workload, budgets=(0, 24, 16)) -> None:
         vp, ll, u32 = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_uint
         errp = ctypes.cast(err.data_ptr(), ctypes.POINTER(ctypes.c_int))
 
+        stages = ep.ep_dispatch_ring_stages()
+
         def load():
-            if L.ring_load(vp(src.data_ptr()), ll(units), u32(chunk), grid, warps, errp) != 0:
+            if L.ring_load(vp(src.data_ptr()), ll(units), u32(chunk), grid, warps, stages, errp) != 0:
                 raise SystemExit("ring load probe: launch failed")
 
         def store():
-            if L.ring_store(vp(dst.data_ptr()), ll(units), u32(chunk), wl.K, grid, warps) != 0:
+            if L.ring_store(vp(dst.data_ptr()), ll(units), u32(chunk), wl.K, grid, warps,
+                            stages) != 0:
                 raise SystemExit("ring store probe: launch failed")
 
         t_load = time_call(load, 20, flush)
@@ -754,7 +767,8 @@ def run_pipeline_model(ep, dev, wl: W.Workload, budgets=(0, 24, 16)) -> None:
         n = -(-units // (grid * warps))
         model = pipeline_time(n, t_load / n, t_store / n)
         print(json.dumps({
-            "workload": wl.name, "num_sms": grid, "chunk_bytes": chunk, "units_per_warp": n,
+            "workload": wl.name, "num_sms": grid, "chunk_bytes": chunk, "ring_stages": stages,
+            "units_per_warp": n,
             "load_stage_us": round(t_load, 1), "store_stage_us": round(t_store, 1),
             "model_pipelined_us": round(model, 1), "model_serial_us": round(t_load + t_store, 1),
             "dispatch_us": round(t_disp, 1), "dispatch_over_model": round(t_disp / model, 3),

@@ -115,6 +115,11 @@ ep_status_t check_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const
     return EP_OK;
 }
 
+// (token, chunk) units the planner aims for per warp before it cuts rows finer.
+#ifndef EP_DISPATCH_UNITS_PER_WARP
+#define EP_DISPATCH_UNITS_PER_WARP 2
+#endif
+
 // Fills the kernel arguments: rows cut into equal 16-byte-multiple chunks
 // that each fit one ring stage (after `reserve` bytes of other shared data).
 // Small batches are cut finer (chunks of at least 512 bytes) until there are
@@ -123,7 +128,7 @@ ep_status_t check_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const
 ep_status_t plan_dispatch(ep::DispatchArgs* a, const uint16_t* x, int64_t T, int64_t H, int K,
                           const int32_t* slot, const float* topk_w, int64_t num_recv,
                           uint16_t* recv_x, float* recv_w, int32_t* recv_src, int32_t* status,
-                          int smem_optin, size_t reserve, int num_sms) {
+                          int smem_optin, size_t reserve, int num_sms, bool fused) {
     a->x = reinterpret_cast<const uint8_t*>(x);
     a->T = T;
     a->row_bytes = static_cast<uint32_t>(H * 2);
@@ -135,16 +140,24 @@ ep_status_t plan_dispatch(ep::DispatchArgs* a, const uint16_t* x, int64_t T, int
     a->recv_w = recv_w;
     a->recv_src = recv_src;
     a->status = status;
-    const uint32_t cap = ep::dispatch_stage_capacity(smem_optin, reserve);
+    a->ring_stages = ep::dispatch_ring_stages(fused);
+    uint32_t cap = ep::dispatch_stage_capacity(smem_optin, reserve, a->ring_stages);
     if (cap < 16) return EP_ERR_UNSUPPORTED;
+#ifdef EP_DISPATCH_MAX_CHUNK
+    if (cap > static_cast<uint32_t>(EP_DISPATCH_MAX_CHUNK)) cap = EP_DISPATCH_MAX_CHUNK;
+#endif
     uint32_t n_chunks = (a->row_bytes + cap - 1) / cap;
     if (T > 0) {
-        const int64_t target_units = 2LL * num_sms * ep::dispatch_warps();
+        const int64_t target_units =
+            static_cast<int64_t>(EP_DISPATCH_UNITS_PER_WARP) * num_sms * ep::dispatch_warps();
         const int64_t n_par = (target_units + T - 1) / T;
         const int64_t n_max = a->row_bytes / 512;  // chunks of at least 512 bytes
         const int64_t n_want = n_par < n_max ? n_par : n_max;
         if (n_want > n_chunks) n_chunks = static_cast<uint32_t>(n_want);
     }
+#ifdef EP_DISPATCH_FORCE_CHUNKS
+    if (static_cast<uint32_t>(EP_DISPATCH_FORCE_CHUNKS) > n_chunks) n_chunks = EP_DISPATCH_FORCE_CHUNKS;
+#endif
     const uint32_t per = (a->row_bytes + n_chunks - 1) / n_chunks;
     a->chunk_bytes = (per + 15u) & ~15u;
     a->n_chunks = (a->row_bytes + a->chunk_bytes - 1) / a->chunk_bytes;
@@ -198,10 +211,12 @@ int64_t ep_dispatch_chunk_bytes(int64_t T, int64_t H, int K) {
     if (!device_limits(&sm_count, &smem_optin)) return -1;
     ep::DispatchArgs a{};
     if (plan_dispatch(&a, nullptr, T, H, K, nullptr, nullptr, 0, nullptr, nullptr, nullptr,
-                      nullptr, smem_optin, 0, sms_in_effect(sm_count)) != EP_OK)
+                      nullptr, smem_optin, 0, sms_in_effect(sm_count), false) != EP_OK)
         return -1;
     return a.chunk_bytes;
 }
+
+int ep_dispatch_ring_stages(void) { return ep::dispatch_ring_stages(false); }
 
 ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, int E,
                                    int32_t* counts, int32_t* offsets, int32_t* slot,
@@ -234,7 +249,7 @@ ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const in
     if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
     ep::DispatchArgs a{};
     st = plan_dispatch(&a, x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src, status,
-                       smem_optin, 0, sms_in_effect(sm_count));
+                       smem_optin, 0, sms_in_effect(sm_count), false);
     if (st != EP_OK) return st;
     return from_cuda(ep::launch_dispatch(a, sms_in_effect(sm_count), smem_optin,
                                          static_cast<cudaStream_t>(stream)));
@@ -257,7 +272,7 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
     ep::DispatchArgs a{};
     const size_t hist = 2 * sizeof(int32_t) * static_cast<size_t>(E);
     st = plan_dispatch(&a, x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src, status,
-                       smem_optin, hist, sms_in_effect(sm_count));
+                       smem_optin, hist, sms_in_effect(sm_count), true);
     if (st != EP_OK) return st;
     ep::FusedLayoutArgs f{};
     f.idx = topk_idx;

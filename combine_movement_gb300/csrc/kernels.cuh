@@ -49,6 +49,7 @@ struct DispatchArgs {
     uint32_t chunk_bytes;  // bytes per row chunk (multiple of 16); last chunk may be shorter
     uint32_t n_chunks;     // chunks per row
     uint32_t stage_bytes;  // shared-memory bytes per ring stage (>= chunk_bytes)
+    int ring_stages;       // ring stages the rows were planned for (host side)
 };
 
 // Routing inputs and layout outputs of the fused layout + dispatch kernel.
@@ -72,7 +73,10 @@ cudaError_t launch_layout_dispatch(const DispatchArgs& a, FusedLayoutArgs f, int
 // Largest ring stage (bytes, multiple of 16) dispatch can use on a device
 // whose per-block shared-memory opt-in limit is `smem_optin`, after
 // reserving `reserve` bytes for other shared data.
-uint32_t dispatch_stage_capacity(int smem_optin, size_t reserve);
+uint32_t dispatch_stage_capacity(int smem_optin, size_t reserve, int stages);
+// Stages of the dispatch ring the next launch will use (fused: the
+// layout-plus-dispatch kernel); plan rows with the same number.
+int dispatch_ring_stages(bool fused);
 
 // Warps per dispatch CTA.
 int dispatch_warps();

@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_layout_launches.argtypes = [i64, i32, i32]
     lib.ep_layout_launches.restype = i32
     lib.ep_dispatch_chunk_bytes.argtypes = [i64, i64, i32]
+    lib.ep_dispatch_ring_stages.argtypes = []
+    lib.ep_dispatch_ring_stages.restype = i32
     lib.ep_dispatch_chunk_bytes.restype = i64
     lib.ep_get_dispatch_layout.argtypes = [p, i64, i32, i32, p, p, p, p, sz, p, p]
     lib.ep_get_dispatch_layout.restype = i32
@@ -144,6 +146,10 @@ def ep_layout_launches(T: int, K: int, E: int) -> int:
 
 def ep_dispatch_chunk_bytes(T: int, H: int, K: int) -> int:
     return int(lib.ep_dispatch_chunk_bytes(T, H, K))
+
+
+def ep_dispatch_ring_stages() -> int:
+    return int(lib.ep_dispatch_ring_stages())
 
 
 def ep_status_string(code: int) -> str:
