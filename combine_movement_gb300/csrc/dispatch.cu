@@ -371,14 +371,16 @@ __global__ void __launch_bounds__(kLsuThreads, 1) dispatch_lsu_kernel(const Disp
 // Ring shape compiled in: stages per warp, loads in flight ahead.
 constexpr int kStages = EP_DISPATCH_STAGES;
 constexpr int kPrefetch = EP_DISPATCH_PREFETCH;
-// While launches overlap (full SM budget) the ring has one stage fewer, so
-// that a dispatch CTA (3 x 8 x ~7 KB = 172 KB) fits beside a CTA of the
-// routing layout (34 KB at 256 experts) on one SM: every dispatch CTA is
-// then resident and waiting when the layout finishes, instead of the ones on
-// the layout's SMs launching only after it ends. On the DeepSeek-V3 prefill
-// step this took 192.8 -> 181.0 us, on T=16384 746 -> 695 us; other shapes
-// and decode were unchanged. Below the full budget launches do not overlap
-// and the 4-stage ring is as fast or up to 2.5 % faster.
+// While launches overlap (full SM budget) the ring has one stage fewer: a
+// dispatch CTA then takes 172 KB of shared memory instead of 229 KB, so the
+// SM does not have to switch to its largest shared-memory configuration
+// (the least L1) for dispatch. With the kernels overlapping that made the
+// DeepSeek-V3 prefill step 192.8 -> 181.0 us (T=16384: 746 -> 695 us);
+// other shapes and decode were unchanged. Forcing the largest configuration
+// on every kernel brought the step back to 191.4 us, and any ring under
+// ~190 KB (6 warps x 4 stages, or 3.5 KB chunks) gave the same gain. Below
+// the full budget launches do not overlap and the 4-stage ring is as fast
+// or up to 2.5 % faster.
 #ifndef EP_DISPATCH_SHARED_STAGES
 #define EP_DISPATCH_SHARED_STAGES 3
 #endif
