@@ -1084,6 +1084,9 @@ def main():
             "tokens_per_s": world * step.T / (ms * 1e-3),
             "dispatch_combine_gbs": moved / ((d + c) * 1e-3) / 1e9,
             "dispatch_combine_frac": moved / ((d + c) * 1e-3) / 1e9 / peak,
+            # the whole step (layout included, kernels overlapping) as bandwidth
+            "step_gbs": (moved + ab["layout"]) / (ms * 1e-3) / 1e9,
+            "step_frac": (moved + ab["layout"]) / (ms * 1e-3) / 1e9 / peak,
             "dispatch_us": 1e3 * d, "combine_us": 1e3 * c, "layout_us": 1e3 * lay,
             "dispatch_gbs": ab["dispatch"] / (d * 1e-3) / 1e9,
             "combine_gbs": ab["combine"] / (c * 1e-3) / 1e9,
