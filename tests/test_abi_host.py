@@ -120,6 +120,27 @@ def test_dispatch_chunk_bytes_plan(ep):
         ep.ep_set_num_sms(0)
 
 
+@pytest.mark.gpu
+def test_ring_depth_follows_budget_and_overlap_mode(ep):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    try:
+        ep.ep_set_num_sms(0)
+        ep.ep_set_launch_overlap(0)
+        assert ep.ep_dispatch_ring_stages() == 3       # full budget: launches overlap
+        ep.ep_set_num_sms(24)
+        assert ep.ep_dispatch_ring_stages() == 4       # shared GPU: no overlap
+        ep.ep_set_launch_overlap(1)
+        assert ep.ep_dispatch_ring_stages() == 3
+        ep.ep_set_num_sms(0)
+        ep.ep_set_launch_overlap(2)
+        assert ep.ep_dispatch_ring_stages() == 4
+    finally:
+        ep.ep_set_num_sms(0)
+        ep.ep_set_launch_overlap(0)
+
+
 def _raw(ep):
     return ep.lib
 

@@ -353,9 +353,11 @@ def test_back_to_back_batches_share_buffers_on_one_stream(ep):
                 y=torch.empty((T, H), dtype=torch.bfloat16).pin_memory()) for _ in cases]
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
-    # budgets with the default launch policy, and 24 SMs with overlapping
-    # launches forced on
-    for b, mode in ((0, 0), (24, 0), (24, 1)):
+    # budgets with the default launch policy, 24 SMs with overlapping
+    # launches forced on, and the full budget with them forced off (each
+    # combination also changes the dispatch ring: 3 stages while launches
+    # overlap, else 4)
+    for b, mode in ((0, 0), (24, 0), (24, 1), (0, 2)):
         ep.ep_set_num_sms(b)
         ep.ep_set_launch_overlap(mode)
         with torch.cuda.stream(s):
