@@ -80,6 +80,13 @@ namespace {
 
 ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 
+// Size limits, tested without forming a product that could overflow int64:
+// T * K (token, expert) pairs and receive rows index with int32, and a row of
+// H bf16 values is measured in uint32 bytes.
+constexpr int64_t kMaxPairs = (int64_t{1} << 31) - 1;
+bool pairs_fit(int64_t T, int K) { return T <= kMaxPairs / K; }
+bool row_fits(int64_t H) { return H <= 0x7FFFFFF0 / 2; }
+
 // Which combine kernel runs: the direct 16-byte gather (0), the bulk-copy
 // staged ring (1), or the ring only at budgets of at most
 // EP_COMBINE_TMA_MAX_SMS SMs (2). Both give identical results.
@@ -103,9 +110,7 @@ ep_status_t check_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const
                            const float* recv_w, const int32_t* recv_src, const int32_t* status) {
     if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || num_recv < 0)
         return EP_ERR_INVALID;
-    if (T * static_cast<int64_t>(K) >= (int64_t{1} << 31) || num_recv >= (int64_t{1} << 31) ||
-        H * 2 > 0x7FFFFFF0)
-        return EP_ERR_UNSUPPORTED;
+    if (!pairs_fit(T, K) || num_recv > kMaxPairs || !row_fits(H)) return EP_ERR_UNSUPPORTED;
     if (T == 0) return EP_OK;
     if (x == nullptr || slot == nullptr || (num_recv > 0 && recv_x == nullptr)) return EP_ERR_INVALID;
     if (recv_w != nullptr && topk_w == nullptr) return EP_ERR_INVALID;
@@ -192,20 +197,22 @@ int ep_num_sms_in_effect(void) {
 }
 
 size_t ep_layout_workspace_bytes(int64_t T, int K, int E) {
-    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return 0;
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || !pairs_fit(T, K))
+        return 0;
     return ep::plan_layout(T * K, E).workspace_bytes;
 }
 
 int ep_layout_launches(int64_t T, int K, int E) {
-    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return -1;
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || !pairs_fit(T, K))
+        return -1;
     const ep::LayoutPlan p = ep::plan_layout(T * K, E);
     if (p.num_tiles == 1 || p.cluster || p.coop) return 1;
     return p.num_tiles <= 512 ? 2 : 3;
 }
 
 int64_t ep_dispatch_chunk_bytes(int64_t T, int64_t H, int K) {
-    if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || H * 2 > 0x7FFFFFF0 ||
-        T * static_cast<int64_t>(K) >= (int64_t{1} << 31))
+    if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || !row_fits(H) ||
+        !pairs_fit(T, K))
         return -1;
     int sm_count = 0, smem_optin = 0;
     if (!device_limits(&sm_count, &smem_optin)) return -1;
@@ -224,7 +231,7 @@ ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, in
                                    void* stream) {
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1) return EP_ERR_INVALID;
     if (E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
-    if (T * static_cast<int64_t>(K) >= (int64_t{1} << 31)) return EP_ERR_UNSUPPORTED;
+    if (!pairs_fit(T, K)) return EP_ERR_UNSUPPORTED;
     if (counts == nullptr || offsets == nullptr) return EP_ERR_INVALID;
     if (T > 0 && (topk_idx == nullptr || slot == nullptr)) return EP_ERR_INVALID;
     if (!aligned(topk_idx, 8) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(slot, 4) ||
@@ -289,9 +296,7 @@ ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv, const int32
                        int32_t* status, void* stream) {
     if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || num_recv < 0)
         return EP_ERR_INVALID;
-    if (T * static_cast<int64_t>(K) >= (int64_t{1} << 31) || num_recv >= (int64_t{1} << 31) ||
-        H * 2 > 0x7FFFFFF0)
-        return EP_ERR_UNSUPPORTED;
+    if (!pairs_fit(T, K) || num_recv > kMaxPairs || !row_fits(H)) return EP_ERR_UNSUPPORTED;
     if (T == 0) return EP_OK;
     if (slot == nullptr || topk_w == nullptr || y == nullptr ||
         (num_recv > 0 && expert_out == nullptr))

@@ -67,7 +67,7 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(const int64_t* topk_idx, i
                                                       void* stream) {
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1) return EP_ERR_INVALID;
     if (E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
-    if (T * static_cast<int64_t>(K) >= (int64_t{1} << 31)) return EP_ERR_UNSUPPORTED;
+    if (T > ((int64_t{1} << 31) - 1) / K) return EP_ERR_UNSUPPORTED;  // T * K must fit int32
     if (counts == nullptr || offsets == nullptr) return EP_ERR_INVALID;
     if (T > 0 && (topk_idx == nullptr || slot == nullptr)) return EP_ERR_INVALID;
     if (!aligned(topk_idx, 8) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(slot, 4) ||

@@ -99,6 +99,34 @@ def test_dispatch_chunk_bytes_rejects_invalid_sizes(ep):
     assert ep.ep_dispatch_chunk_bytes(4096, 7168, 33) == -1  # K above the limit
     assert ep.ep_dispatch_chunk_bytes(-1, 7168, 8) == -1
     assert ep.ep_dispatch_chunk_bytes(1 << 28, 7168, 8) == -1  # T*K overflows int32 slots
+    assert ep.ep_dispatch_chunk_bytes(1 << 62, 7168, 8) == -1  # T*K would overflow int64 too
+
+
+def test_sizes_near_int64_limits_are_refused_before_any_device_call(ep):
+    """Limits are checked without forming T*K or H*2, so sizes whose products
+    overflow int64 are refused too (UNSUPPORTED), never wrapped into range."""
+    lib = ep.lib
+    A = 0x10000  # a fake, 16-byte aligned "device" address; never dereferenced
+    UNSUP = ep.EP_ERR_UNSUPPORTED
+    for T in ((1 << 28), (1 << 62) + 3, (1 << 63) - 1):
+        assert ep.ep_layout_workspace_bytes(T, 8, 256) == 0
+        assert ep.ep_layout_launches(T, 8, 256) == -1
+        assert lib.ep_get_dispatch_layout(A, T, 8, 256, A, A, A, None, 0, None, None) == UNSUP
+        assert lib.ep_get_dispatch_layout_noalloc(A, T, 8, 256, A, A, A, None, None) == UNSUP
+        assert lib.ep_dispatch(A, T, 7168, 8, A, None, 8, A, None, None, None, None) == UNSUP
+        assert lib.ep_combine(A, 8, A, A, T, 7168, 8, A, None, None) == UNSUP
+    for H in ((1 << 30), (1 << 62), (1 << 63) - 8):
+        assert lib.ep_dispatch(A, 16, H, 8, A, None, 8, A, None, None, None, None) == UNSUP
+        assert lib.ep_combine(A, 8, A, A, 16, H, 8, A, None, None) == UNSUP
+        assert ep.ep_dispatch_chunk_bytes(16, H, 8) == -1
+    # the boundary: 2^31 - 1 (token, expert) pairs pass the size check and
+    # stop at the null buffers (INVALID); one token more is refused
+    T_max = ((1 << 31) - 1) // 8
+    assert lib.ep_dispatch(None, T_max, 7168, 8, None, None, 8, None, None, None, None,
+                           None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch(None, T_max + 1, 7168, 8, None, None, 8, None, None, None, None,
+                           None) == UNSUP
+    assert lib.ep_combine(A, (1 << 31), A, A, 16, 7168, 8, A, None, None) == UNSUP  # num_recv
 
 
 @pytest.mark.gpu
