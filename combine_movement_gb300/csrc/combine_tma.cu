@@ -186,7 +186,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) combine_tma_kernel(const Co
         if (leader) ok = mbar_wait_bounded(bar0 + 8u * s, static_cast<uint32_t>((j / NS) & 1));
         ok = __shfl_sync(kFullMask, ok, leader_lane);
         if (!ok) {
-            if (leader) set_status(a.status, EP_ERR_TIMEOUT);
+            if (leader) {
+                set_status(a.status, EP_ERR_TIMEOUT);
+                mbar_drain_bounded<NS>(bar0, j, j + P < n ? j + P : n - 1);
+            }
             break;
         }
         const uint32_t off = static_cast<uint32_t>(u - t * n_c) * kChunk;

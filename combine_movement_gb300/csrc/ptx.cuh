@@ -95,6 +95,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// After a ring wait gave up: wait again, each with the same bound, for the
+// loads of ring units `first` .. `last` that may still be in flight (unit i
+// lands in stage i % NS and completes phase (i / NS) & 1 of its barrier), so
+// no bulk copy writes shared memory after the CTA has exited. Returns whether
+// all of them arrived.
+template <int NS>
+__device__ __forceinline__ bool mbar_drain_bounded(uint32_t bar0, int64_t first, int64_t last,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
+    bool all = true;
+    for (int64_t i = first; i <= last; ++i)
+        all &= mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(i % NS),
+                                 static_cast<uint32_t>((i / NS) & 1), limit_ns);
+    return all;
+}
+
 // ---- L2 cache policies ---------------------------------------------------
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

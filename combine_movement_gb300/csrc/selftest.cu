@@ -3,9 +3,11 @@
 // Every mbarrier wait in the kernels gives up after a time limit and records
 // EP_ERR_TIMEOUT in the caller's status word instead of spinning forever.
 // ep_selftest_wait_timeout makes that happen on purpose, safely: one warp
-// waits on a freshly initialised mbarrier that nothing will ever complete,
-// with a short limit, so the wait runs out, the status is written and the
-// kernel returns. The context stays usable.
+// waits on the first of a ring of three freshly initialised mbarriers that
+// nothing will ever complete, with a short limit, so the wait runs out and
+// the status is written. It then drains the ring the way the copy kernels do
+// after a timeout (one more bounded wait per stage that could still have a
+// load in flight) and returns. The context stays usable.
 #include <cuda_runtime.h>
 
 #include "../../include/ep.h"
@@ -13,13 +15,18 @@
 
 namespace {
 
+constexpr int kRing = 3;
+
 __global__ void wait_timeout_kernel(int32_t* status, uint64_t limit_ns) {
-    __shared__ __align__(8) uint64_t bar;
-    const uint32_t b = ep::smem_u32(&bar);
+    __shared__ __align__(8) uint64_t bar[kRing];
+    const uint32_t b = ep::smem_u32(bar);
     if (threadIdx.x == 0) {
-        ep::mbar_init(b, 1);  // one arrival expected; none will come
+        for (int s = 0; s < kRing; ++s) ep::mbar_init(b + 8u * s, 1);  // no arrival will come
         ep::fence_mbar_init();
-        if (!ep::mbar_wait_bounded(b, 0, limit_ns)) ep::set_status(status, EP_ERR_TIMEOUT);
+        if (!ep::mbar_wait_bounded(b, 0, limit_ns)) {
+            ep::set_status(status, EP_ERR_TIMEOUT);
+            ep::mbar_drain_bounded<kRing>(b, 0, kRing - 1, limit_ns);
+        }
     }
 }
 

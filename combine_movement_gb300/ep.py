@@ -100,8 +100,17 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, what: str = "") -> Optional[int]
     return t.data_ptr() if t.numel() > 0 else None
 
 
+# The current stream's raw handle, read without building a torch.cuda.Stream
+# object (about 2 us less per call on the host). Every call passes a CUDA
+# tensor first, so CUDA is initialised by the time this runs.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
+        if _raw_stream is not None and _cur_device is not None:
+            return _raw_stream(_cur_device()) or None
         stream = torch.cuda.current_stream()
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream or None

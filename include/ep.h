@@ -226,8 +226,10 @@ EP_API ep_status_t ep_get_dispatch_layout_noalloc(const int64_t* topk_idx, int64
 /* Self-test of the failure path: launches one warp that waits, for at most
  * `limit_ns` nanoseconds (1 .. 2e9), on an mbarrier nothing completes, so the
  * bounded wait gives up and writes EP_ERR_TIMEOUT to *status (the way every
- * wait in the kernels ends if a copy never arrives) and the kernel returns.
- * For tests; it changes nothing else. */
+ * wait in the kernels ends if a copy never arrives). Like the copy kernels
+ * after a timeout, it then waits once more, with the same bound, on each stage
+ * of its three-stage ring that could still have a load in flight, and returns
+ * after about four limits. For tests; it changes nothing else. */
 EP_API ep_status_t ep_selftest_wait_timeout(int32_t* status, uint64_t limit_ns, void* stream);
 
 /* Synchronises `stream`, then returns the device status word (an

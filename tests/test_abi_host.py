@@ -169,6 +169,22 @@ def test_ring_depth_follows_budget_and_overlap_mode(ep):
         ep.ep_set_launch_overlap(0)
 
 
+@pytest.mark.gpu
+def test_binding_passes_the_current_stream(ep):
+    """With no stream argument the binding passes torch's current stream of
+    the current device (the legacy default stream as NULL)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.zeros(1, device="cuda")
+    assert ep._stream(None) == (torch.cuda.current_stream().cuda_stream or None)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert ep._stream(None) == s.cuda_stream
+    assert ep._stream(s) == s.cuda_stream
+    assert ep._stream(None) == (torch.cuda.current_stream().cuda_stream or None)
+
+
 def _raw(ep):
     return ep.lib
 

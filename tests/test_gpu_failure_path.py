@@ -26,7 +26,8 @@ def test_bounded_wait_times_out_and_context_survives(ep):
     t0 = time.perf_counter()
     ep.ep_selftest_wait_timeout(status, 2_000_000)  # 2 ms
     assert ep.ep_get_status(status) == ep.EP_ERR_TIMEOUT
-    assert time.perf_counter() - t0 >= 0.002
+    # the first wait and the drain of the three-stage ring, each bounded
+    assert time.perf_counter() - t0 >= 4 * 0.002
     # the device is still usable: a normal layout + dispatch + combine
     from combine_movement_gb300 import workloads as W
     import oracle
