@@ -92,8 +92,10 @@ typedef enum {
 /* SM budget, after DeepEP's Buffer.set_num_sms ([DeepEP-TMA] "Minimal SM
  * Occupancy Configuration"): dispatch and combine launch one CTA per SM on at
  * most this many SMs. 0 means all SMs. Values above the device's SM count
- * are clamped at launch. Returns the stored budget, or -1 (and changes
- * nothing) if num_sms < 0. */
+ * are clamped at launch. The layout is not budgeted (like the pages' budget,
+ * this one covers the copy kernels): it runs a few microseconds on one
+ * block, one 8-CTA cluster, or one block per tile of the routing table.
+ * Returns the stored budget, or -1 (and changes nothing) if num_sms < 0. */
 EP_API int ep_set_num_sms(int num_sms);
 
 /* The stored SM budget (0 = all). */
