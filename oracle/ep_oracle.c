@@ -130,6 +130,8 @@ void oracle_combine(const uint16_t* expert_out, const int32_t* slot,
             float acc = 0.0f;
 #if ORACLE_MUTANT == 1
             for (int k = 0; k < K - 1; ++k) {              /* planted: last term dropped */
+#elif ORACLE_MUTANT == 10
+            for (int k = K - 1; k >= 0; --k) {             /* planted: descending k */
 #else
             for (int k = 0; k < K; ++k) {
 #endif
@@ -143,6 +145,8 @@ void oracle_combine(const uint16_t* expert_out, const int32_t* slot,
                 float v = oracle_bf16_to_f32(expert_out[(int64_t)s * H + h]);
 #if ORACLE_MUTANT == 7
                 acc = fmaf(w, v, -acc);                    /* planted: sign error */
+#elif ORACLE_MUTANT == 9
+                acc = acc + w * v;                         /* planted: two roundings */
 #else
                 acc = fmaf(w, v, acc);
 #endif

@@ -10,7 +10,9 @@ show that each mistake is caught.
 from __future__ import annotations
 
 import itertools
+import math
 import os
+from fractions import Fraction
 
 import numpy as np
 import torch
@@ -261,6 +263,107 @@ def check_combine_error_bound(o) -> None:
         assert np.all(np.abs(yf - exact) <= chain + half_ulp + 1e-30), np.max(np.abs(yf - exact) - chain - half_ulp)
 
 
+# Exact model of the combine arithmetic, independent of C's fmaf and of any
+# float conversion routine: every fused multiply-add is the exact rational
+# w*v + acc rounded once to binary32 (round to nearest, ties to even), and
+# the final narrowing rounds that binary32 value once to bfloat16 (8
+# significant bits, same exponent range). Both are IEEE 754 round-to-nearest
+# written out over Fractions.
+
+def _round_binary(q: Fraction, p: int, emin: int = -126, emax: int = 127):
+    """q rounded to the nearest binary float with p significant bits and
+    exponents emin..emax (gradual underflow), ties to even; a Fraction, or
+    +-inf on overflow. Zero comes back as Fraction(0)."""
+    if q == 0:
+        return Fraction(0)
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if a < Fraction(2) ** e:
+        e -= 1
+    elif a >= Fraction(2) ** (e + 1):
+        e += 1
+    quantum = Fraction(2) ** (max(e, emin) - (p - 1))
+    m = a / quantum
+    n = m.numerator // m.denominator
+    rest = m - n
+    if rest > Fraction(1, 2) or (rest == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    v = n * quantum
+    if v >= Fraction(2) ** (emax + 1):
+        return math.copysign(math.inf, q)
+    return v if q > 0 else -v
+
+
+def _bf16_value(bits: int) -> Fraction:
+    """Exact value of a finite bfloat16 bit pattern (sign, 8-bit exponent, 7-bit fraction)."""
+    sign = -1 if bits & 0x8000 else 1
+    ex = (bits >> 7) & 0xFF
+    fr = bits & 0x7F
+    assert ex != 0xFF
+    if ex == 0:
+        return sign * Fraction(fr, 1 << 7) * Fraction(2) ** -126
+    return sign * (1 + Fraction(fr, 1 << 7)) * Fraction(2) ** (ex - 127)
+
+
+def _bf16_bits_of(v: Fraction) -> int:
+    """Bits of a bfloat16-representable value (via binary32, where it is exact)."""
+    f = np.array([float(v)], dtype=np.float32)
+    assert Fraction(float(f[0])) == v
+    return int(f.view(np.uint32)[0] >> 16)
+
+
+def _combine_exact(eo_bits: np.ndarray, slot: np.ndarray, w: np.ndarray) -> np.ndarray:
+    T, K = slot.shape
+    H = eo_bits.shape[1]
+    y = np.zeros((T, H), dtype=np.uint16)
+    for t in range(T):
+        for h in range(H):
+            acc = Fraction(0)
+            for k in range(K):
+                s = int(slot[t, k])
+                if s < 0:
+                    continue
+                acc = _round_binary(Fraction(float(w[t, k])) * _bf16_value(int(eo_bits[s, h])) + acc, 24)
+            y[t, h] = _bf16_bits_of(_round_binary(acc, 8))
+    return y
+
+
+def check_combine_exact(o) -> None:
+    """The oracle's combine, bit for bit, against the exact model: random
+    weights and rows (some entries masked), and two hand-derived tokens where
+    the k order and the single rounding of each fma decide the bf16 output."""
+    rng = np.random.default_rng(29)
+    for T, H, K, mask in [(16, 24, 8, 0.0), (12, 16, 5, 0.3), (8, 16, 1, 0.0)]:
+        E = 24
+        idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int64)
+        idx[rng.random((T, K)) < mask] = -1
+        _, offsets, slot, _ = o.layout(idx, E)
+        R = int(offsets[-1])
+        eo = torch.from_numpy(rng.standard_normal((R, H), dtype=np.float32) * 4).to(torch.bfloat16)
+        eob = _bf16_bits(eo)
+        w = rng.standard_normal((T, K), dtype=np.float32)
+        assert np.array_equal(o.combine(eob, slot, w), _combine_exact(eob, slot, w))
+
+    # Two tokens, one expert row per (t, k), row r = 3t + k.
+    one, big = 0x3F80, 0x4980                   # 1.0 and 2^20 in bfloat16
+    small = 0x3F81                              # 1 + 2^-7
+    slot = np.array([[0, 1, 2], [3, 4, -1]], dtype=np.int32)
+    eob = np.zeros((5, 8), dtype=np.uint16)
+    # token 0: rows small, 2^20, -2^20 with weights 1. In k order the first
+    # sum rounds small to the 1/8 grid of 2^20, so the result is 1.0 (a
+    # reversed order would give small itself).
+    eob[0], eob[1], eob[2] = small, big, big | 0x8000
+    # token 1: w0 = -(1 + 2^-7 + 2^-20) times 1.0, then w1 = 1 + 2^-20 times
+    # (1 + 2^-7): the exact sum is 2^-27, which a fused multiply-add keeps;
+    # rounding the product first would cancel to +0.
+    eob[3], eob[4] = one, small
+    w = np.array([[1.0, 1.0, 1.0],
+                  [-(1 + 2.0 ** -7 + 2.0 ** -20), 1 + 2.0 ** -20, 0.0]], dtype=np.float32)
+    want = np.array([[0x3F80] * 8, [0x3200] * 8], dtype=np.uint16)   # 1.0 and 2^-27
+    assert np.array_equal(_combine_exact(eob, slot, w), want)
+    assert np.array_equal(o.combine(eob, slot, w), want)
+
+
 # --------------------------------------------------------------------------
 # pipeline model
 
@@ -305,5 +408,6 @@ ALL_CHECKS = {
     "dispatch": check_dispatch,
     "combine_closed_forms": check_combine_closed_forms,
     "combine_error_bound": check_combine_error_bound,
+    "combine_exact": check_combine_exact,
     "pipeline": check_pipeline,
 }

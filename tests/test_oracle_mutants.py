@@ -9,14 +9,16 @@ import oracle_pins
 
 # mutant id -> the pins expected to catch it
 MUTANTS = {
-    1: ["combine_closed_forms", "combine_error_bound"],  # last k term dropped
-    2: ["combine_closed_forms", "combine_error_bound"],  # weight index reversed
+    1: ["combine_closed_forms", "combine_error_bound", "combine_exact"],  # last k term dropped
+    2: ["combine_closed_forms", "combine_error_bound", "combine_exact"],  # weight index reversed
     3: ["layout_hand", "layout_bruteforce", "layout_random"],  # unstable order
     4: ["layout_hand", "layout_random"],  # off-by-one offsets
     5: ["dispatch"],  # wrong source row
     6: ["bf16"],  # truncating conversion
     7: ["combine_closed_forms", "combine_error_bound"],  # sign error in the chain
     8: ["pipeline"],  # min instead of max
+    9: ["combine_exact"],  # multiply and add rounded separately
+    10: ["combine_exact"],  # k descending
 }
 
 
