@@ -20,7 +20,8 @@
 // Units whose K slots are all valid and which lie wholly inside the row take
 // an unpredicated body whose fmas go in packed fp32 pairs (fma.rn.f32x2,
 // the same rounding per element), for every K <= 8. Below the wide budgets
-// each CTA runs as many threads as the registers allow (768 or 1024).
+// each lane keeps two or four column blocks of loads in flight (see
+// narrow_shape).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,27 +32,40 @@
 namespace ep {
 namespace {
 
-// Two compiled shapes (threads per CTA, column blocks per unit), chosen by
-// the SM budget: with many SMs, fewer threads with two blocks in flight each
-// win; with few SMs, as many threads as the registers allow (more loads in
-// flight per SM).
+// Compiled shapes (threads per CTA, column blocks per unit), chosen by the
+// SM budget: with many SMs (HBM-bound), 384 threads with two blocks each;
+// with few SMs, each SM's read rate follows the bytes it keeps in flight,
+// so each lane takes two (K = 1: four) blocks per unit, 2K (4K) independent
+// loads, with as many threads as the registers then allow without spilling.
 #ifndef EP_COMBINE_WIDE_THREADS
 #define EP_COMBINE_WIDE_THREADS 384
 #endif
 #ifndef EP_COMBINE_WIDE_UNROLL
 #define EP_COMBINE_WIDE_UNROLL 2
 #endif
-// Narrow shape (one column block per unit): as many threads per CTA as the
-// register budget (65536 / threads) allows while the unpredicated body keeps
-// its K row loads in registers without spilling. For K >= 6 the rows are
-// addressed by 32-bit slot index instead of a 64-bit pointer per k (one more
-// multiply-add per load, 8-16 fewer registers), which buys the extra threads.
-// Measured best at 16-48 SMs for K = 2, 4, 5, 6 and 8. K > 8 (generic path):
-// 768.
-constexpr int narrow_threads(int KT) {
-    return KT == 0 ? 768 : KT <= 6 ? 1024 : 768;
+// Narrow shape per K: threads per CTA, column blocks per unit, and whether
+// expert rows are addressed by 32-bit slot index (one more multiply-add per
+// load, fewer registers) instead of a 64-bit pointer per k. Each was the
+// fastest measured at 16-48 SMs (thread counts that split evenly over the
+// SM's four schedulers). K > 8 (generic path): 768 threads, one block.
+struct NarrowShape {
+    int threads;
+    int unroll;
+    bool slot_rows;
+};
+constexpr NarrowShape narrow_shape(int KT) {
+    switch (KT) {
+        case 1: return {1024, 4, true};
+        case 2: return {1024, 2, false};
+        case 3: return {1024, 2, false};
+        case 4: return {896, 2, true};
+        case 5: return {640, 2, true};
+        case 6: return {640, 2, true};
+        case 7: return {512, 2, true};
+        case 8: return {512, 2, true};
+        default: return {768, 1, false};
+    }
 }
-constexpr bool narrow_slot_rows(int KT) { return KT >= 6; }
 // Budgets of at least this many SMs use the wide shape.
 #ifndef EP_COMBINE_WIDE_MIN_SMS
 #define EP_COMBINE_WIDE_MIN_SMS 96
@@ -260,8 +274,8 @@ cudaError_t launch_k(const CombineArgs& a, int num_sms, cudaStream_t stream) {
     if (num_sms >= EP_COMBINE_WIDE_MIN_SMS)
         return launch_shape<KT, EP_COMBINE_WIDE_THREADS, EP_COMBINE_WIDE_UNROLL, (KT > 0), false>(
             a, num_sms, stream);
-    return launch_shape<KT, narrow_threads(KT), 1, (KT > 0), narrow_slot_rows(KT)>(a, num_sms,
-                                                                                  stream);
+    constexpr NarrowShape n = narrow_shape(KT);
+    return launch_shape<KT, n.threads, n.unroll, (KT > 0), n.slot_rows>(a, num_sms, stream);
 }
 
 }  // namespace

@@ -204,6 +204,20 @@ def test_edge_shapes(ep, T, H, E, K, mask):
         assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=b), ref)
 
 
+@pytest.mark.parametrize("K", range(1, 9))
+@pytest.mark.parametrize("mask", [0.0, 0.2])
+def test_narrow_combine_shapes_every_k(ep, K, mask):
+    """Below the wide budgets each K has its own combine shape (threads,
+    two or four 512-byte column blocks per unit, row addressing). Rows of
+    7184 bytes hold whole units plus a 16-byte tail, so both the unpredicated
+    body and the predicated one run, with and without masked entries."""
+    inp = _custom(200, 3592, 32, K, seed=40 + K, mask=mask)
+    num_recv = int((inp.topk_idx >= 0).sum()) + 2
+    ref = oracle_path(inp, num_recv, 1.5)
+    for b in (3, 24):
+        assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=b), ref)
+
+
 def _fuzz_cases(n=24, seed=2024):
     """Seeded random shapes: T, H (a multiple of 8), E, K <= min(E, 32),
     masking, routing and SM budget drawn at random, sized so the oracle
