@@ -8,9 +8,9 @@
 // at +0.0f, one fused multiply-add per k in ascending k (entries with slot < 0
 // skipped), one bf16 round-to-nearest-even per output element.
 //
-// Mapping: persistent grid of one CTA per SM (the SM budget). A unit is one
-// or two 512-byte column blocks of one token row (a block is 32 lanes x 16
-// bytes); every warp
+// Mapping: persistent grid of one CTA per SM (the SM budget). A unit is one,
+// two or four 512-byte column blocks of one token row (a block is 32 lanes x
+// 16 bytes); every warp
 // takes a contiguous, equal range of units, so the load is balanced to within
 // one unit whatever T and the budget. For each token the warp reads slot and
 // weight once (lanes k < K) and broadcasts them with warp shuffles; each lane
@@ -19,9 +19,8 @@
 // writes 16 bytes, so every warp store is a coalesced 512-byte row segment.
 // Units whose K slots are all valid and which lie wholly inside the row take
 // an unpredicated body whose fmas go in packed fp32 pairs (fma.rn.f32x2,
-// the same rounding per element), for every K <= 8. Below the wide budgets
-// each lane keeps two or four column blocks of loads in flight (see
-// narrow_shape).
+// the same rounding per element), for every K <= 8. Each lane keeps two or
+// four column blocks of loads in flight (see combine_shape).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -32,28 +31,22 @@
 namespace ep {
 namespace {
 
-// Compiled shapes (threads per CTA, column blocks per unit), chosen by the
-// SM budget: with many SMs (HBM-bound), 384 threads with two blocks each;
-// with few SMs, each SM's read rate follows the bytes it keeps in flight,
-// so each lane takes two (K = 1: four) blocks per unit, 2K (4K) independent
-// loads, with as many threads as the registers then allow without spilling.
-#ifndef EP_COMBINE_WIDE_THREADS
-#define EP_COMBINE_WIDE_THREADS 384
-#endif
-#ifndef EP_COMBINE_WIDE_UNROLL
-#define EP_COMBINE_WIDE_UNROLL 2
-#endif
-// Narrow shape per K: threads per CTA, column blocks per unit, and whether
-// expert rows are addressed by 32-bit slot index (one more multiply-add per
-// load, fewer registers) instead of a 64-bit pointer per k. Each was the
-// fastest measured at 16-48 SMs (thread counts that split evenly over the
-// SM's four schedulers). K > 8 (generic path): 768 threads, one block.
-struct NarrowShape {
+// Compiled shape per K: threads per CTA, 512-byte column blocks per unit,
+// and whether expert rows are addressed by 32-bit slot index (one more
+// multiply-add per load, fewer registers) instead of a 64-bit pointer per
+// k. A lane issues all K x blocks loads of a unit before its fmas, and on a
+// small SM budget each SM's read rate follows the bytes it keeps in flight,
+// so each lane takes two (K = 1: four) blocks per unit with as many threads
+// as the registers then hold without spilling. Each entry was the fastest
+// measured at 16-48 SMs (thread counts that split evenly over the SM's four
+// schedulers), and at 96 and 152 SMs, where HBM bounds K >= 4, it is as
+// fast as or faster than 384 threads x 2 blocks.
+struct CombineShape {
     int threads;
     int unroll;
     bool slot_rows;
 };
-constexpr NarrowShape narrow_shape(int KT) {
+constexpr CombineShape combine_shape(int KT) {
     switch (KT) {
         case 1: return {1024, 4, true};
         case 2: return {1024, 2, false};
@@ -63,13 +56,16 @@ constexpr NarrowShape narrow_shape(int KT) {
         case 6: return {640, 2, true};
         case 7: return {512, 2, true};
         case 8: return {512, 2, true};
-        default: return {768, 1, false};
+        default: return {768, 1, false};  // generic path, K > 8, below kGenericWideSms
     }
 }
-// Budgets of at least this many SMs use the wide shape.
-#ifndef EP_COMBINE_WIDE_MIN_SMS
-#define EP_COMBINE_WIDE_MIN_SMS 96
-#endif
+// The generic path (K > 8) runs 384 threads x 2 blocks from this many SMs up.
+constexpr int kGenericWideSms = 96;
+// A batch too small to give every budgeted SM one CTA of its K's shape (a
+// decode step at a large budget) runs 384 threads x 2 blocks instead: 12
+// warps per CTA spread it over more SMs.
+constexpr int kSmallThreads = 384;
+constexpr int kSmallUnroll = 2;
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr uint32_t kColBytes = 512;  // row bytes one warp covers per column block
@@ -269,13 +265,22 @@ cudaError_t launch_shape(const CombineArgs& a, int num_sms, cudaStream_t stream)
     return launch_dependent(kern, grid, kThreads, kExclusiveSmem, stream, a);
 }
 
+// CTAs a shape needs for one unit per warp.
+int64_t ctas_for_shape(const CombineArgs& a, int threads, int unroll) {
+    const int64_t unit_bytes = static_cast<int64_t>(kColBytes) * unroll;
+    const int64_t units = a.T * ((a.row_bytes + unit_bytes - 1) / unit_bytes);
+    const int64_t warps = threads / 32;
+    return (units + warps - 1) / warps;
+}
+
 template <int KT>
 cudaError_t launch_k(const CombineArgs& a, int num_sms, cudaStream_t stream) {
-    if (num_sms >= EP_COMBINE_WIDE_MIN_SMS)
-        return launch_shape<KT, EP_COMBINE_WIDE_THREADS, EP_COMBINE_WIDE_UNROLL, (KT > 0), false>(
-            a, num_sms, stream);
-    constexpr NarrowShape n = narrow_shape(KT);
-    return launch_shape<KT, n.threads, n.unroll, (KT > 0), n.slot_rows>(a, num_sms, stream);
+    constexpr CombineShape c = combine_shape(KT);
+    const bool small = KT == 0 ? num_sms >= kGenericWideSms
+                               : ctas_for_shape(a, c.threads, c.unroll) < num_sms;
+    if (small)
+        return launch_shape<KT, kSmallThreads, kSmallUnroll, (KT > 0), false>(a, num_sms, stream);
+    return launch_shape<KT, c.threads, c.unroll, (KT > 0), c.slot_rows>(a, num_sms, stream);
 }
 
 }  // namespace
