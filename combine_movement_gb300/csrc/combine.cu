@@ -10,17 +10,16 @@
 //
 // Mapping: persistent grid of one CTA per SM (the SM budget). A unit is one,
 // two or four 512-byte column blocks of one token row (a block is 32 lanes x
-// 16 bytes); every warp
-// takes a contiguous, equal range of units, so the load is balanced to within
-// one unit whatever T and the budget. For each token the warp reads slot and
-// weight once (lanes k < K) and broadcasts them with warp shuffles; each lane
-// then issues K independent 16-byte loads (read-only path, no L1 allocation),
-// widens bf16 to fp32 exactly (bit shift), runs the fma chain in k order and
-// writes 16 bytes, so every warp store is a coalesced 512-byte row segment.
-// Units whose K slots are all valid and which lie wholly inside the row take
-// an unpredicated body whose fmas go in packed fp32 pairs (fma.rn.f32x2,
-// the same rounding per element), for every K <= 8. Each lane keeps two or
-// four column blocks of loads in flight (see combine_shape).
+// 16 bytes); every warp takes a contiguous, equal range of units, so the
+// load is balanced to within one unit whatever T and the budget. For each
+// token the warp reads slot and weight once (lanes k < K) and broadcasts
+// them with warp shuffles; each lane then issues K independent 16-byte loads
+// per column block of the unit (read-only path, no L1 allocation), widens
+// bf16 to fp32 exactly (bit shift), runs the fma chain in k order and writes
+// 16 bytes per block, so every warp store is a coalesced 512-byte row
+// segment. Units whose K slots are all valid and which lie wholly inside the
+// row take an unpredicated body whose fmas go in packed fp32 pairs
+// (fma.rn.f32x2, the same rounding per element), for every K <= 8.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
