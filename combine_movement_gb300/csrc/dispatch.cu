@@ -203,10 +203,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
-    if (FUSED) fused_layout(a, f, smem, units, nw_total);
     const int64_t u0 = units * gw / nw_total;
     const int64_t n = units * (gw + 1) / nw_total - u0;
-    if (n <= 0) return;
 
     // L2 policies: x is read once (evict first); the receive rows are
     // written once and next read by the experts (normal).
@@ -246,7 +244,12 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
                                                               : 0.0f;
     };
 
+    // The rows of x do not depend on the layout, so the first loads go out
+    // before the fused kernel computes it (every thread of the CTA then
+    // takes part in that, whatever its own share of units).
     for (int64_t j = 0; j < P && j < n; ++j) issue_load(j);
+    if (FUSED) fused_layout(a, f, smem, units, nw_total);
+    if (n <= 0) return;
 
     int64_t tok = u0 / a.n_chunks;
     int32_t s_cur = load_slot(tok), s_next = load_slot(tok + 1);
