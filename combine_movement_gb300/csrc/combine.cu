@@ -68,6 +68,7 @@ constexpr int kSmallUnroll = 2;
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr uint32_t kColBytes = 512;  // row bytes one warp covers per column block
+constexpr int kGenericBatch = 8;     // k entries per batch of loads in the generic path
 
 __device__ __forceinline__ uint4 ld_expert(const uint8_t* p) {
     uint4 v;
@@ -228,14 +229,30 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
                 for (int k = 0; k < KR; ++k)
                     if (on[k] && in_row[j]) fma8(acc[j], wk[k], v[j][k]);
         } else {
-            for (int k = 0; k < K; ++k) {
-                const int32_t sk = __shfl_sync(kFullMask, s_lane, k);
-                const float w = __shfl_sync(kFullMask, w_lane, k);
-                if (sk < 0) continue;
-                const uint8_t* row = a.expert_out + static_cast<int64_t>(sk) * a.row_bytes;
+            // Any K <= 32, kGenericBatch entries of k at a time: all their
+            // loads are issued before their fmas, which still run in k order.
+            for (int k0 = 0; k0 < K; k0 += kGenericBatch) {
+                uint4 v[kUnroll][kGenericBatch];
+                float wq[kGenericBatch];
+                bool onq[kGenericBatch];
 #pragma unroll
-                for (int j = 0; j < kUnroll; ++j)
-                    if (in_row[j]) fma8(acc[j], w, ld_expert(row + col0 + j * kColBytes));
+                for (int q = 0; q < kGenericBatch; ++q) {
+                    const int k = k0 + q;  // < 32 + kGenericBatch; lanes read mod 32
+                    const int32_t sk = __shfl_sync(kFullMask, s_lane, k & 31);
+                    wq[q] = __shfl_sync(kFullMask, w_lane, k & 31);
+                    onq[q] = k < K && sk >= 0;
+                    const uint8_t* row =
+                        a.expert_out + static_cast<int64_t>(onq[q] ? sk : 0) * a.row_bytes;
+#pragma unroll
+                    for (int j = 0; j < kUnroll; ++j)
+                        v[j][q] = (onq[q] && in_row[j]) ? ld_expert(row + col0 + j * kColBytes)
+                                                        : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int q = 0; q < kGenericBatch; ++q)
+#pragma unroll
+                    for (int j = 0; j < kUnroll; ++j)
+                        if (onq[q] && in_row[j]) fma8(acc[j], wq[q], v[j][q]);
             }
         }
         uint8_t* yrow = a.y + t * static_cast<int64_t>(a.row_bytes);
