@@ -466,54 +466,241 @@ def time_call(fn, reps: int, flush=None) -> float:
     return statistics.median(ts)
 
 
-def decode_latency(ep, dev, budgets=(16, 24, 0)) -> dict:
+def empty_launch_us(reps: int = 200) -> float:
+    """Event-to-event time of one empty kernel launched the same way as a
+    timed call (after a spin): the launch and event overhead every single-
+    kernel figure below carries."""
+    return time_call(lambda: torch.cuda._sleep(0), reps)
+
+
+def per_sm_ceilings(dev, budgets) -> dict:
+    """Write-only and read-only rates of plain 16-byte streaming kernels (the
+    probes of --ceilings) on n SMs, one 1024-thread CTA per SM: over 1 GiB
+    (DRAM) and over 64 MB, 20 launches back to back (L2-resident, like a
+    warm decode step). GB/s for the n SMs together; empty where nvcc or the
+    probe library is unavailable."""
+    import ctypes
+    try:
+        L = _probe_lib()
+    except Exception as e:  # noqa: BLE001 - reported, not fatal
+        log(f"per-SM ceilings unavailable: {e}")
+        return {}
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    sms_all = torch.cuda.get_device_properties(dev).multi_processor_count
+    big = 1 << 30
+    a = torch.ones(big, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def best(fn, nbytes, reps=8, per_event=1):
+        """Best of `reps` timings; each times `per_event` launches back to
+        back between two events (amortising the event and launch overhead
+        over short launches)."""
+        ts = []
+        for i in range(reps + 2):
+            s_ = torch.cuda.Event(enable_timing=True)
+            e_ = torch.cuda.Event(enable_timing=True)
+            s_.record()
+            for _ in range(per_event):
+                if fn() != 0:
+                    raise RuntimeError("probe launch failed")
+            e_.record()
+            torch.cuda.synchronize()
+            if i >= 2:
+                ts.append(s_.elapsed_time(e_) / per_event)
+        return nbytes / (min(ts) * 1e-3) / 1e9
+
+    out = {}
+    small = 64 << 20
+    for b in budgets:
+        n = min(b or sms_all, sms_all)
+        g, blk = (n, 1024) if n < sms_all else (8 * n, 512)
+        r = {
+            "write_dram_gbs": best(lambda: L.bw_write(vp(a.data_ptr()), sz(big), g, blk), big),
+            "read_dram_gbs": best(lambda: L.bw_read(vp(a.data_ptr()), sz(big), vp(sink.data_ptr()),
+                                                    g, blk), big),
+            "write_l2_gbs": best(lambda: L.bw_write(vp(a.data_ptr()), sz(small), g, blk), small,
+                                 5, 20),
+            "read_l2_gbs": best(lambda: L.bw_read(vp(a.data_ptr()), sz(small), vp(sink.data_ptr()),
+                                                  g, blk), small, 5, 20),
+        }
+        out[n] = {k: round(v, 1) for k, v in r.items()}
+    del a
+    torch.cuda.empty_cache()
+    return out
+
+
+def decode_latency(ep, dev, budgets=(16, 24, 0), ceilings: dict | None = None) -> dict:
     """Per-call latency of layout + dispatch + combine on the decode
-    workload (T=128, H=7168, E=256, top-8; 16.5 MB, L2-resident when warm)."""
+    workload (T=128, H=7168, E=256, top-8; 16.5 MB, L2-resident when warm),
+    at each SM budget: the whole step (warm and cold, both step forms, as a
+    CUDA graph, back to back), each kernel timed alone, and the step with
+    launch overlap forced on. Each kernel's figure is also given net of the
+    event-to-event time of an empty launch, and against what its n SMs can
+    move (write ceiling for dispatch, read ceiling for combine; L2-resident
+    probes, since the warm step's data sits in L2)."""
     wl = W.DECODE
     step = Step(ep, W.make_inputs(wl), dev)
     flush = _Flusher(dev)
     ab = algorithmic_bytes(wl.T, wl.H, wl.K, wl.E, wl.T * wl.K)
-    out = {"workload": wl_desc(wl)}
+    rows = wl.T * wl.K * 2 * wl.H  # receive-row bytes each copy kernel writes or reads
+    sms_all = torch.cuda.get_device_properties(dev).multi_processor_count
+    overhead = empty_launch_us()
+    out = {"workload": wl_desc(wl), "empty_launch_us": round(overhead, 2)}
+    mode0 = ep.ep_get_launch_overlap()
     for b in budgets:
+        n = min(b or sms_all, sms_all)
         ep.ep_set_num_sms(b)
         warm = time_call(lambda: step.run(step.b), 200)
         cold = time_call(lambda: step.run(step.b), 30, flush)
         fwarm = time_call(lambda: step.run_fused(step.b), 200)
         fcold = time_call(lambda: step.run_fused(step.b), 30, flush)
+        k_lay = time_call(lambda: step.layout(step.b), 200)
+        k_dis = time_call(lambda: step.dispatch(step.b), 200)
+        k_com = time_call(lambda: step.combine(step.b), 200)
         # the same three calls captured once into a CUDA graph and replayed
         # (one host launch per step)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             step.run(step.b, torch.cuda.current_stream())
         gwarm = time_call(g.replay, 200)
+        ep.ep_set_launch_overlap(1)
+        owarm = time_call(lambda: step.run(step.b), 200)
+        ep.ep_set_launch_overlap(mode0)
 
-        def back_to_back(fn, n=500):
+        def back_to_back(fn, n_=500):
             for _ in range(5):
                 fn()
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
-            for _ in range(n):
+            for _ in range(n_):
                 fn()
             e1.record()
             torch.cuda.synchronize()
-            return e0.elapsed_time(e1) / n * 1e3
+            return e0.elapsed_time(e1) / n_ * 1e3
         out_b2b = back_to_back(lambda: step.run(step.b))
         graph_b2b = back_to_back(g.replay)
-        out[f"sms_{b or 'all'}"] = {
+        net = {k: max(v - overhead, 1e-3) for k, v in
+               (("layout", k_lay), ("dispatch", k_dis), ("combine", k_com))}
+        entry = {
+            "num_sms": n,
             "warm_us": round(warm, 2), "cold_us": round(cold, 2),
             "cold_gbs": round((ab["dispatch"] + ab["combine"]) / (cold * 1e-6) / 1e9, 1),
             "fused_warm_us": round(fwarm, 2), "fused_cold_us": round(fcold, 2),
             "graph_warm_us": round(gwarm, 2),
+            "launch_overlap_forced_warm_us": round(owarm, 2),
             # steps issued back to back from the host (no spin in between):
             # the eager calls are bound by the host's launch rate, the graph
             # is not
             "back_to_back_us": round(out_b2b, 2), "graph_back_to_back_us": round(graph_b2b, 2),
+            # each kernel alone, warm, event to event (includes one launch)
+            "kernel_us": {"layout": round(k_lay, 2), "dispatch": round(k_dis, 2),
+                          "combine": round(k_com, 2)},
+            "kernel_net_us": {k: round(v, 2) for k, v in net.items()},
         }
+        c = (ceilings or {}).get(n)
+        if c:
+            w_cap, r_cap = c["write_l2_gbs"], c["read_l2_gbs"]
+            entry["budget_ceilings_gbs"] = {"write": w_cap, "read": r_cap,
+                                            "source": f"16-byte streaming probes on {n} SMs, "
+                                                      "64 MB L2-resident"}
+            # receive rows written by dispatch / read by combine, per net second
+            entry["dispatch_write_frac_of_budget_ceiling"] = round(
+                rows / (net["dispatch"] * 1e-6) / 1e9 / w_cap, 3)
+            entry["combine_read_frac_of_budget_ceiling"] = round(
+                rows / (net["combine"] * 1e-6) / 1e9 / r_cap, 3)
+        out[f"sms_{b or 'all'}"] = entry
         del g
     ep.ep_set_num_sms(0)
     return out
+
+
+def budget_ceiling_frac(c: dict | None, s: dict, step) -> dict | None:
+    """Dispatch's receive-row writes and combine's receive-row reads on a
+    budget of n SMs, as fractions of the n SMs' own DRAM write-only and
+    read-only ceilings (c: per_sm_ceilings entry for n)."""
+    if not c:
+        return None
+    rows = step.R * 2 * step.H
+    w = rows / (s["dispatch_us"] * 1e-6) / 1e9
+    r = rows / (s["combine_us"] * 1e-6) / 1e9
+    return {"num_sms": s["num_sms"],
+            "dispatch_write_gbs": round(w, 1), "write_ceiling_gbs": c["write_dram_gbs"],
+            "dispatch_frac": round(w / c["write_dram_gbs"], 3),
+            "combine_read_gbs": round(r, 1), "read_ceiling_gbs": c["read_dram_gbs"],
+            "combine_frac": round(r / c["read_dram_gbs"], 3),
+            "ceiling_source": "16-byte streaming write-only / read-only kernels over 1 GiB "
+                              f"on {s['num_sms']} SMs (one 1024-thread CTA per SM)"}
+
+
+def time_workload(ep, dev, wl: W.Workload, budget: int, steps: int, warmup: int,
+                  peak: float) -> dict:
+    """One workload at one SM budget: K steps back to back (events only
+    around the loop), the same step captured once in a CUDA graph and
+    replayed K times, and a pass with events between the kernels for the
+    per-kernel medians. Inputs resident in HBM."""
+    step = Step(ep, W.make_inputs(wl), dev)
+    sms_all = torch.cuda.get_device_properties(dev).multi_processor_count
+    ep.ep_set_num_sms(budget)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        run = time_steps(step, steps, warmup, False, stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step.run(step.b, stream)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    st = ep.ep_get_status(step.b.status)
+    ep.ep_set_num_sms(0)
+    if st != 0:
+        raise SystemExit(f"{wl.name}: device status {st}: {ep.ep_status_string(st)}")
+    ab = algorithmic_bytes(wl.T, wl.H, wl.K, wl.E, step.R)
+    ms = run["total_ms"] / steps
+    gms = e0.elapsed_time(e1) / steps
+    med = {k: statistics.median(run[f"{k}_ms"]) * 1e3 for k in ("layout", "dispatch", "combine")}
+    moved = ab["dispatch"] + ab["combine"]
+    d_c = med["dispatch"] + med["combine"]
+    return {
+        "workload": wl_desc(wl), "num_sms": min(budget or sms_all, sms_all),
+        "steps": steps,
+        "ms_per_step": round(ms, 5), "tokens_per_s": round(wl.T / (ms * 1e-3)),
+        "graph_ms_per_step": round(gms, 5), "graph_tokens_per_s": round(wl.T / (gms * 1e-3)),
+        "step_gbs": round((moved + ab["layout"]) / (min(ms, gms) * 1e-3) / 1e9, 1),
+        "kernel_us_median": {k: round(v, 2) for k, v in med.items()},
+        "dispatch_gbs": round(ab["dispatch"] / (med["dispatch"] * 1e-6) / 1e9, 1),
+        "combine_gbs": round(ab["combine"] / (med["combine"] * 1e-6) / 1e9, 1),
+        "dispatch_combine_gbs": round(moved / (d_c * 1e-6) / 1e9, 1),
+        "dispatch_combine_frac_of_peak": round(moved / (d_c * 1e-6) / 1e9 / peak, 3),
+        "algorithmic_bytes": ab,
+    }
+
+
+def run_workloads(ep, dev, budget: int, steps: int, warmup: int) -> None:
+    """Every workload of the measurement plan at all SMs and at `budget`
+    SMs: one JSON line each (time_workload), with the SM clock sampled over
+    the workload's runs. Small workloads are L2-resident between steps (no
+    flush); the large ones are many times the L2."""
+    peak, peak_src = peak_hbm()
+    wls = [W.TINY, W.DEEPSEEK_PREFILL, W.SKEWED, W.DECODE,
+           W.sweep(max(W.SWEEP_T), max(W.SWEEP_H))]
+    for wl in wls:
+        for b in (0, budget):
+            with ClockSampler(dev.index or 0) as cs:
+                r = time_workload(ep, dev, wl, b, steps, warmup, peak)
+            r["peak_gbs"] = peak
+            r["peak_source"] = peak_src
+            r["clocks"] = cs.summary()
+            print(json.dumps(r), flush=True)
+            torch.cuda.empty_cache()
 
 
 def run_sweep(ep, dev, budgets) -> None:
@@ -878,11 +1065,12 @@ extern "C" int run_fma(void* out, int grid, int iters, void* stream) {
 """
 
 
-def run_overlap(ep, dev, budgets=(16, 24, 48), steps: int = 60) -> None:
+def run_overlap(ep, dev, wl: W.Workload, budgets=(16, 24, 48), steps: int = 60) -> None:
     """For each budget n: time (a) an ALU-bound kernel on 152-n SMs alone,
-    (b) `steps` dispatch+combine steps (DeepSeek-V3 prefill, layout done
-    beforehand) at budget n alone, (c) both at once on two streams. One JSON
-    line per budget, with the SM clock sampled during (c)."""
+    (b) `steps` dispatch+combine steps of `wl` (layout done beforehand) at
+    budget n alone, (c) both at once on two streams. Decode-size workloads
+    run the whole step (layout included) and 20x the steps. One JSON line
+    per budget and launch-overlap mode, with the SM clock sampled during (c)."""
     import ctypes
     import tempfile
     tmp = tempfile.mkdtemp(prefix="ep_overlap_")
@@ -895,7 +1083,10 @@ def run_overlap(ep, dev, budgets=(16, 24, 48), steps: int = 60) -> None:
     L.run_fma.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     out = torch.zeros(1, device=dev)
-    step = Step(ep, W.make_inputs(W.DEEPSEEK_PREFILL), dev)
+    step = Step(ep, W.make_inputs(wl), dev)
+    small = wl.T * wl.K * wl.H * 2 < (64 << 20)  # receive rows under 64 MB
+    if small:
+        steps *= 20
     s_move = torch.cuda.Stream(dev, priority=-1)
     s_comp = torch.cuda.Stream(dev)
 
@@ -904,6 +1095,8 @@ def run_overlap(ep, dev, budgets=(16, 24, 48), steps: int = 60) -> None:
 
     def movement(n_steps):
         for _ in range(n_steps):
+            if small:
+                step.layout(step.b, s_move)
             step.dispatch(step.b, s_move)
             step.combine(step.b, s_move)
 
@@ -947,6 +1140,7 @@ def run_overlap(ep, dev, budgets=(16, 24, 48), steps: int = 60) -> None:
         sampler.__exit__(None, None, None)
         flops = 4 * 2 * iters * 1024 * grid
         print(json.dumps({
+            "workload": wl.name, "step": "layout+dispatch+combine" if small else "dispatch+combine",
             "num_sms_movement": n, "num_sms_alu": grid, "steps": steps,
             "launch_overlap": "auto (off below the full budget)" if mode == 0 else "forced on",
             "movement_ms_per_step_alone": round(move_ms / steps, 4),
@@ -974,8 +1168,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: the T x H x SM-budget sweep, one JSON line each")
     ap.add_argument("--overlap", action="store_true",
-                    help="instead of the bench line: dispatch+combine on n SMs next to an "
-                         "ALU-bound kernel on the other SMs (n = 16, 24, 48)")
+                    help="instead of the bench line: dispatch+combine of --workload on n SMs "
+                         "next to an ALU-bound kernel on the other SMs (n = 16, 24, 48)")
     ap.add_argument("--pipeline-model", action="store_true",
                     help="two-stage pipeline model of the dispatch ring vs the measured kernel")
     ap.add_argument("--ceilings", action="store_true",
@@ -983,6 +1177,13 @@ def main():
     ap.add_argument("--only-main", action="store_true",
                     help="for profiling: only the all-SM timed loop (no 24-SM, fused, e2e or "
                          "decode passes)")
+    ap.add_argument("--decode", action="store_true",
+                    help="instead of the bench line: only the decode-latency breakdown "
+                         "(16, 24, all SMs) as one JSON line")
+    ap.add_argument("--workloads", action="store_true",
+                    help="instead of the bench line: one JSON line per workload (tiny, "
+                         "DeepSeek-V3 prefill, skewed Zipf, decode, largest sweep point) at "
+                         "all SMs and at --budget-sms")
     ap.add_argument("--ncu-budgets", action="store_true",
                     help="for profiling: one layout+dispatch+combine step at each SM budget "
                          "(16, 24, 48, all), after one warm-up step")
@@ -1012,7 +1213,7 @@ def main():
 
     if args.overlap:
         if rank == 0:
-            run_overlap(ep, dev)
+            run_overlap(ep, dev, wl)
         return
 
     if args.pipeline_model:
@@ -1033,6 +1234,18 @@ def main():
             torch.cuda.synchronize(dev)
         ep.ep_set_num_sms(0)
         print(json.dumps({"ncu_budgets": [16, 24, 48, "all"], "status": ep.ep_get_status(step.b.status)}))
+        return
+
+    if args.decode:
+        if rank == 0:
+            budgets = (16, args.budget_sms, 0) if args.budget_sms != 16 else (16, 0)
+            ceil = per_sm_ceilings(dev, budgets)
+            print(json.dumps(decode_latency(ep, dev, budgets, ceil)), flush=True)
+        return
+
+    if args.workloads:
+        if rank == 0:
+            run_workloads(ep, dev, args.budget_sms, args.steps, args.warmup)
         return
 
     if args.sweep:
@@ -1064,7 +1277,8 @@ def main():
     fused_budget = time_fused_steps(step, args.steps, args.warmup, dist_on, stream)
     ep.ep_set_num_sms(0)
     e2e = time_e2e(step, inp, max(3, min(args.steps, 200)), 3)
-    decode = decode_latency(ep, dev) if rank == 0 else None
+    ceil = per_sm_ceilings(dev, (16, args.budget_sms, 0)) if rank == 0 else {}
+    decode = decode_latency(ep, dev, (16, args.budget_sms, 0), ceil) if rank == 0 else None
     st = ep.ep_get_status(step.b.status)
     if st != 0:
         raise SystemExit(f"device status {st}: {ep.ep_status_string(st)}")
@@ -1157,6 +1371,12 @@ def main():
                 for k in ("dispatch", "combine")
                 for tag, r in (("all_sms", s_all), (f"sms_{args.budget_sms}", s_bud))
             },
+            # the budgeted kernels against what that many SMs can move at all:
+            # receive-row bytes dispatch writes (combine reads) per second over
+            # the write-only (read-only) rate of plain streaming kernels on the
+            # same number of SMs, measured in this run
+            "budget_ceiling_frac": budget_ceiling_frac(
+                ceil.get(min(args.budget_sms, sms_all)), s_bud, step),
             "e2e": {
                 "value": world * step.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "ms_per_step": e2e_ms,

@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/ep.h"
+#include "combine_math.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -69,48 +70,6 @@ constexpr int kSmallUnroll = 2;
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr uint32_t kColBytes = 512;  // row bytes one warp covers per column block
 constexpr int kGenericBatch = 8;     // k entries per batch of loads in the generic path
-
-__device__ __forceinline__ uint4 ld_expert(const uint8_t* p) {
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
-}
-
-// acc[i] = fma(w, float(bf16 element i of v), acc[i]) for the 8 elements of v.
-__device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4& v) {
-    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(w, __uint_as_float(q[i] << 16), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(w, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
-    }
-}
-
-// Same arithmetic as fma8 with packed fp32 pairs: acc2[i] holds elements
-// 2i and 2i+1; fma.rn.f32x2 rounds each half exactly like fmaf.
-__device__ __forceinline__ void fma8_x2(uint64_t (&acc2)[4], float w, const uint4& v) {
-    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-    uint64_t w2;
-    asm("mov.b64 %0, {%1, %1};" : "=l"(w2) : "f"(w));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint64_t e2;
-        asm("mov.b64 %0, {%1, %2};" : "=l"(e2) : "r"(q[i] << 16), "r"(q[i] & 0xFFFF0000u));
-        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[i]) : "l"(w2), "l"(e2));
-    }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint4 round8(const float (&acc)[8]) {
-    return make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-}
 
 // KT > 0: K == KT known at compile time (slots, row pointers and weights in
 // registers). KT == 0: any K <= 32, broadcast per unit. A unit is UN
@@ -182,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
 #pragma unroll
             for (int k = 0; k < KR; ++k)
 #pragma unroll
-                for (int j = 0; j < kUnroll; ++j) v[j][k] = ld_expert(row(k) + col0 + j * kColBytes);
+                for (int j = 0; j < kUnroll; ++j) v[j][k] = ld_nc_v4_dep(row(k) + col0 + j * kColBytes);
             float acc[kUnroll][8];
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
@@ -222,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
             for (int k = 0; k < KR; ++k)
 #pragma unroll
                 for (int j = 0; j < kUnroll; ++j)
-                    if (on[k] && in_row[j]) v[j][k] = ld_expert(row(k) + col0 + j * kColBytes);
+                    if (on[k] && in_row[j]) v[j][k] = ld_nc_v4_dep(row(k) + col0 + j * kColBytes);
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j)
 #pragma unroll
@@ -245,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
                         a.expert_out + static_cast<int64_t>(onq[q] ? sk : 0) * a.row_bytes;
 #pragma unroll
                     for (int j = 0; j < kUnroll; ++j)
-                        v[j][q] = (onq[q] && in_row[j]) ? ld_expert(row + col0 + j * kColBytes)
+                        v[j][q] = (onq[q] && in_row[j]) ? ld_nc_v4_dep(row + col0 + j * kColBytes)
                                                         : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll

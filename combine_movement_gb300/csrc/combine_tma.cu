@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/ep.h"
+#include "combine_math.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -59,20 +60,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
     return v;
-}
-
-__device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4& v) {
-    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(w, __uint_as_float(q[i] << 16), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(w, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
-    }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 template <int KT>
@@ -212,8 +199,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) combine_tma_kernel(const Co
 #pragma unroll
                 for (int k = 0; k < KT; ++k)
                     if (on[k]) fma8(acc, wk[k], v[k]);
-                st_v4(yrow + col, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+                st_v4(yrow + col, round8(acc));
             }
         }
         __syncwarp();

@@ -229,6 +229,7 @@ ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, in
                                    int32_t* counts, int32_t* offsets, int32_t* slot,
                                    void* workspace, size_t workspace_bytes, int32_t* status,
                                    void* stream) {
+    ep::ApiRange range("ep_get_dispatch_layout");
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1) return EP_ERR_INVALID;
     if (E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
     if (!pairs_fit(T, K)) return EP_ERR_UNSUPPORTED;
@@ -249,6 +250,7 @@ ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, in
 ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const int32_t* slot,
                         const float* topk_w, int64_t num_recv, uint16_t* recv_x, float* recv_w,
                         int32_t* recv_src, int32_t* status, void* stream) {
+    ep::ApiRange range("ep_dispatch");
     ep_status_t st = check_dispatch(x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src,
                                     status);
     if (st != EP_OK || T == 0) return st;
@@ -266,6 +268,7 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
                                int K, int E, const float* topk_w, int64_t num_recv, int32_t* counts,
                                int32_t* offsets, int32_t* slot, uint16_t* recv_x, float* recv_w,
                                int32_t* recv_src, int32_t* status, void* stream) {
+    ep::ApiRange range("ep_layout_dispatch");
     if (E < 1) return EP_ERR_INVALID;
     if (E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
     if (counts == nullptr || offsets == nullptr || !aligned(counts, 4) || !aligned(offsets, 4))
@@ -294,6 +297,7 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
 ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv, const int32_t* slot,
                        const float* topk_w, int64_t T, int64_t H, int K, uint16_t* y,
                        int32_t* status, void* stream) {
+    ep::ApiRange range("ep_combine");
     if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || num_recv < 0)
         return EP_ERR_INVALID;
     if (!pairs_fit(T, K) || num_recv > kMaxPairs || !row_fits(H)) return EP_ERR_UNSUPPORTED;

@@ -8,7 +8,37 @@
 #include <cstdint>
 #include <utility>
 
+// NVTX ranges around the C ABI calls, so a profiler's timeline (Nsight
+// Systems) attributes each launch to ep_get_dispatch_layout, ep_dispatch,
+// ep_combine, ... The NVTX 3 header is self-contained; with no profiler
+// attached a range costs a check of one function pointer. -DEP_NVTX=0
+// compiles them out.
+#ifndef EP_NVTX
+#define EP_NVTX 1
+#endif
+#if EP_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace ep {
+
+// Scoped NVTX range named after the entry point (a string literal).
+struct ApiRange {
+    explicit ApiRange(const char* name) {
+#if EP_NVTX
+        nvtxRangePushA(name);
+#else
+        (void)name;
+#endif
+    }
+    ~ApiRange() {
+#if EP_NVTX
+        nvtxRangePop();
+#endif
+    }
+    ApiRange(const ApiRange&) = delete;
+    ApiRange& operator=(const ApiRange&) = delete;
+};
 
 // ---- layout ---------------------------------------------------------------
 

@@ -427,13 +427,18 @@ __global__ void __launch_bounds__(1024) layout_cluster_kernel(
 //            earlier tiles; scan the totals across experts; write every
 //            entry's final slot once. Block 0 writes counts and offsets.
 // The barrier: each block publishes a 64-bit target value in its flag word
-// and waits (bounded in time) until every block's flag holds it. The target
-// is the generation word kept in the workspace plus one, under a per-process
-// salt in the upper half (its top bit set, so no stale pair of counts can
-// spell it); block 0 stores the new generation once every block has passed
+// and waits (bounded in time) until every block's flag holds it. The
+// workspace starts with two words, an owner tag and a generation. Every
+// process draws one random epoch in [2^63, 2^63 + 2^62) (top bit set, so no
+// stale pair of 32-bit tile counts can spell a target). If the owner tag is
+// this process's epoch, the target is the stored generation plus one;
+// otherwise (a fresh or foreign workspace) it is the epoch plus one. Block 0
+// stores the new generation and the owner tag once every block has passed
 // the barrier (or, after a timed-out wait, the giving-up block does). So the
-// barrier words need no clearing between calls, and a replayed launch with
-// identical arguments still waits for fresh flags.
+// barrier words need no clearing between calls, a replayed launch with
+// identical arguments still waits for fresh flags, and within a process the
+// targets only grow (2^62 calls before the counter could wrap), so no flag
+// left by an earlier call, however long ago, can equal a later target.
 __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -463,7 +468,7 @@ __device__ bool grid_barrier(uint64_t* flags, int nblocks, uint64_t target) {
 }
 
 __global__ void __launch_bounds__(1024) layout_coop_kernel(const int64_t* __restrict__ idx, int64_t N, int E, int rounds,
-                                   uint64_t* sync, int32_t* tile_counts, uint32_t salt,
+                                   uint64_t* sync, int32_t* tile_counts, uint64_t epoch,
                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                    int32_t* __restrict__ slot, int32_t* status) {
     extern __shared__ int32_t run[];  // [warps][E]; phase 2 reuses the first 2E words
@@ -475,9 +480,10 @@ __global__ void __launch_bounds__(1024) layout_coop_kernel(const int64_t* __rest
     const int kbits = key_bits_for(E);
 
     griddep_launch_dependents();  // all blocks are resident (cooperative launch)
-    // generation: read before the barrier, replaced after it
-    const uint64_t g = *reinterpret_cast<volatile uint64_t*>(sync);
-    const uint64_t g0 = (g >> 32) == salt ? g : (static_cast<uint64_t>(salt) << 32);
+    // owner tag and generation: read before the barrier, replaced after it
+    const uint64_t owner = reinterpret_cast<volatile uint64_t*>(sync)[0];
+    const uint64_t g = reinterpret_cast<volatile uint64_t*>(sync)[1];
+    const uint64_t g0 = (owner == epoch && g >= epoch) ? g : epoch;
     const uint64_t target = g0 + 1;
 
     // phase 1 ------------------------------------------------------------
@@ -519,15 +525,19 @@ __global__ void __launch_bounds__(1024) layout_coop_kernel(const int64_t* __rest
 #pragma unroll
     for (int r = 0; r < kMaxRounds; ++r)
         if (r < rounds && key[r] >= 0) rank[r] += my[key[r]];
-    if (!grid_barrier(sync + 1, nt, target)) {
+    if (!grid_barrier(sync + 2, nt, target)) {
         // leave the generation past every flag this call may have published
         if (threadIdx.x == 0) {
             set_status(status, EP_ERR_TIMEOUT);
-            st_release_u64(sync, target);
+            st_release_u64(sync + 1, target);
+            st_release_u64(sync, epoch);
         }
         return;
     }
-    if (tile_id == 0 && threadIdx.x == 0) st_release_u64(sync, target);
+    if (tile_id == 0 && threadIdx.x == 0) {
+        st_release_u64(sync + 1, target);
+        st_release_u64(sync, epoch);
+    }
 
     // phase 2: per expert, its total and the rows of earlier tiles. Q threads
     // share an expert (tiles q, q+Q, ...), each with all its loads in flight
@@ -632,24 +642,31 @@ LayoutPlan plan_layout(int64_t N, int E) {
     }
     p.coop = p.num_tiles > 1 && p.num_tiles <= kCoopMaxTiles;
     if (p.num_tiles > 1) {
-        // [generation][flag x tiles] | tile_counts[tiles][E]
+        // [owner][generation][flag x tiles] | tile_counts[tiles][E]
         auto up16 = [](size_t v) { return (v + 15) & ~static_cast<size_t>(15); };
-        p.counts_off = up16(sizeof(uint64_t) * (1 + static_cast<size_t>(p.num_tiles)));
+        p.counts_off = up16(sizeof(uint64_t) * (2 + static_cast<size_t>(p.num_tiles)));
         p.workspace_bytes = p.counts_off + sizeof(int32_t) * static_cast<size_t>(E) * p.num_tiles;
     }
     return p;
 }
 
 namespace {
-// Per-process salt of the layout barriers' generation values (top bit set).
-uint32_t barrier_salt() {
-    static const uint32_t salt = [] {
+// Per-process epoch of the layout barriers' generation values: random, in
+// [2^63, 2^63 + 2^62).
+uint64_t barrier_epoch() {
+    static const uint64_t epoch = [] {
         const uint64_t t = static_cast<uint64_t>(
             std::chrono::steady_clock::now().time_since_epoch().count());
-        const uint64_t h = (t ^ (static_cast<uint64_t>(getpid()) << 21)) * 0x9E3779B97F4A7C15ull;
-        return static_cast<uint32_t>(h >> 32) | 0x80000000u;
+        uint64_t h = t ^ (static_cast<uint64_t>(getpid()) << 21);
+        // splitmix64 finaliser: spreads the clock and pid bits over the word
+        h ^= h >> 30;
+        h *= 0xBF58476D1CE4E5B9ull;
+        h ^= h >> 27;
+        h *= 0x94D049BB133111EBull;
+        h ^= h >> 31;
+        return (uint64_t{1} << 63) | (h & ((uint64_t{1} << 62) - 1));
     }();
-    return salt;
+    return epoch;
 }
 }  // namespace
 
@@ -700,9 +717,9 @@ cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,
                                                static_cast<int>(kRunSmemBudget));
         if (err != cudaSuccess) return err;
         int rounds = p.rounds;
-        uint32_t salt = barrier_salt();
+        uint64_t epoch = barrier_epoch();
         void* args[] = {(void*)&idx,  (void*)&N,      (void*)&E,       (void*)&rounds,
-                        (void*)&sync, (void*)&tile_counts, (void*)&salt, (void*)&counts,
+                        (void*)&sync, (void*)&tile_counts, (void*)&epoch, (void*)&counts,
                         (void*)&offsets, (void*)&slot, (void*)&status};
         err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(layout_coop_kernel),
                                           dim3(p.num_tiles), dim3(threads), args, p.smem, stream);

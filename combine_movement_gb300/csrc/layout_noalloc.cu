@@ -7,21 +7,26 @@
 // reserved pool). A latency-critical pipeline cannot afford one either:
 // cudaMalloc and cudaFree may synchronise the whole device and stall every
 // stream that is in flight. For them the multi-tile layout's scratch (the
-// per-(expert, tile) counts, kLayoutScratchBytes at most) lives in a
-// file-scope __device__ array instead. Every GPU that loads the library
-// holds that array until the process exits.
+// barrier words and the per-(tile, expert) counts, kLayoutScratchBytes at
+// most) lives in a file-scope __device__ array instead. Every GPU that loads
+// the library holds that array until the process exits.
 //
 // Set-up: host code cannot pass the array's name to a kernel (on the host it
 // is only a stand-in symbol, not a device address), so the first call on
-// each device, with that device current, looks its address up once with
-// cudaGetSymbolAddress and caches it. That first call should therefore be
-// made before any stream capture.
+// each device, with that device current, looks its address up with
+// cudaGetSymbolAddress and caches it, together with the unique id of the
+// CUDA context it was looked up in. A later call in another context of that
+// device (after cudaDeviceReset, which destroys the primary context and
+// with it the module that holds the array) looks it up again. Each lookup
+// should therefore be made outside any stream capture: make the first call
+// on a device, and the first one after a reset, before capturing.
 //
 // Sharing: every call uses the same array. Each call rewrites the counts it
-// reads, and the single generation word it carries from call to call is
-// valid from any starting value, so nothing has to start at zero; but calls
-// that overlap on the GPU (different streams, or different host threads)
-// race on the array and must be ordered by the caller.
+// reads, and the barrier words it carries from call to call are valid from
+// any starting value, so nothing has to start at zero; but calls that
+// overlap on the GPU (different streams, or different host threads) race on
+// the array and must be ordered by the caller.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -37,23 +42,71 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) int32_t g_layout_scratch[kLayoutScratchBytes / sizeof(int32_t)];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+// Driver entry points for the current context's unique id (CUDA 12.0+),
+// fetched through the runtime so the library links no driver library.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of g_layout_scratch on the current device (looked up once
-// per device).
+struct ScratchCache {
+    void* addr = nullptr;
+    unsigned long long ctx_id = 0;
+};
+
+std::mutex g_scratch_mu;
+ScratchCache g_scratch[kMaxDevices];
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+bool g_entry_points_tried = false;
+
+// Unique id of the current CUDA context; 0 when no context is current yet.
+// Returns false (and leaves the cache keyed by device alone) where the
+// driver offers no context ids.
+bool current_context_id(unsigned long long* out) {
+    *out = 0;
+    if (!g_entry_points_tried) {
+        g_entry_points_tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+    }
+    if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+        g_ctx_get_id(ctx, &id) == CUDA_SUCCESS)
+        *out = id;
+    return true;
+}
+
+// Device address of g_layout_scratch on the current device, looked up once
+// per device and context.
 ep_status_t scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return EP_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchCache& c = g_scratch[dev];
+    unsigned long long id = 0;
+    const bool keyed = current_context_id(&id);
+    if (c.addr == nullptr || (keyed && (id == 0 || id != c.ctx_id))) {
+        // (the lookup makes the device's primary context current if it is
+        // not yet, so the id taken after it is the context of the address)
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_layout_scratch) != cudaSuccess || p == nullptr)
             return EP_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        c.addr = p;
+        c.ctx_id = 0;
+        if (keyed) current_context_id(&c.ctx_id);
     }
-    *out = g_scratch_addr[dev];
+    *out = c.addr;
     return EP_OK;
 }
 
@@ -65,6 +118,7 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(const int64_t* topk_idx, i
                                                       int E, int32_t* counts, int32_t* offsets,
                                                       int32_t* slot, int32_t* status,
                                                       void* stream) {
+    ep::ApiRange range("ep_get_dispatch_layout_noalloc");
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1) return EP_ERR_INVALID;
     if (E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
     if (T > ((int64_t{1} << 31) - 1) / K) return EP_ERR_UNSUPPORTED;  // T * K must fit int32

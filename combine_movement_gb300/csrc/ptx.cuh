@@ -176,6 +176,18 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     return v;
 }
 
+// The same load without `volatile`, so the compiler may schedule it freely
+// among other loads. Only for addresses computed from data loaded after
+// griddep_wait() (a combine row address comes from its slot), which keeps it
+// behind that wait.
+__device__ __forceinline__ uint4 ld_nc_v4_dep(const void* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)

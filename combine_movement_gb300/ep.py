@@ -32,6 +32,25 @@ EP_MAX_TOPK = 32
 EP_MAX_EXPERTS = 4096
 
 
+def _header_define(name: str) -> int:
+    """Integer value of a #define in include/ep.h (the C ABI's own header),
+    so sizes the binding checks against cannot drift from it."""
+    import re
+    hdr = os.path.join(os.path.dirname(_PKG), "include", "ep.h")
+    with open(hdr) as f:
+        m = re.search(rf"^#define\s+{name}\s+(.+?)\s*$", f.read(), re.M)
+    if m is None:
+        raise ImportError(f"{name} is not defined in {hdr}")
+    expr = re.sub(r"(?<=\d)[uUlL]+\b", "", m.group(1))
+    if not re.fullmatch(r"[\d\s()<+*x]+", expr):
+        raise ImportError(f"{name} in {hdr}: unexpected expression {m.group(1)!r}")
+    return int(eval(expr, {"__builtins__": {}}))  # digits, parentheses, <<, +, * only
+
+
+# Size of the static scratch array behind ep_get_dispatch_layout_noalloc.
+EP_NOALLOC_SCRATCH_BYTES = _header_define("EP_NOALLOC_SCRATCH_BYTES")
+
+
 class EPError(RuntimeError):
     def __init__(self, code: int, what: str):
         super().__init__(f"{what}: {ep_status_string(code)} (code {code})")
@@ -193,7 +212,6 @@ def ep_get_dispatch_layout_noalloc(topk_idx: torch.Tensor, num_experts: int,
     _check(code, "ep_get_dispatch_layout_noalloc")
 
 
-EP_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 def ep_dispatch(x: torch.Tensor, slot: torch.Tensor, recv_x: torch.Tensor,

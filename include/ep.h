@@ -147,10 +147,12 @@ EP_API int ep_dispatch_ring_stages(void);
  *   offsets    int32 [E+1]    out: first row of each expert; offsets[E] = R
  *   slot       int32 [T][K]   out: receive row of (t,k), -1 if skipped
  *   workspace  device scratch of ep_layout_workspace_bytes(T,K,E) bytes,
- *              16-byte aligned. It carries a small generation word from one
- *              call to the next (the kernels' grid barriers use it); any
- *              initial content is valid, so it never needs clearing. Calls
- *              that share a workspace must not overlap on the GPU.
+ *              16-byte aligned. It carries two small words (owner tag and
+ *              generation) from one call to the next for the kernels' grid
+ *              barrier; any initial content is valid, so it never needs
+ *              clearing, and within a process the barrier's targets never
+ *              repeat. Calls that share a workspace must not overlap on the
+ *              GPU.
  *   status     int32 device word, nullable (device errors: BAD_EXPERT)
  * T == 0 is valid (counts and offsets are zeroed). */
 EP_API ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, int E,
@@ -214,8 +216,11 @@ EP_API ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv,
  *  - Limit: sizes whose ep_layout_workspace_bytes(T,K,E) exceeds
  *    EP_NOALLOC_SCRATCH_BYTES are rejected with EP_ERR_UNSUPPORTED.
  *  - Set-up: the first call on each device (with that device current) looks
- *    up the array's device address; make that first call before any stream
- *    capture.
+ *    up the array's device address and caches it with the id of the current
+ *    CUDA context; make that first call before any stream capture. A
+ *    cudaDeviceReset destroys the context and the array with it: the next
+ *    call on that device (again outside any capture) looks the address up
+ *    anew, and the array's contents start over.
  *  - Sharing: all calls share the array. Calls that overlap on the GPU (other
  *    streams or host threads) race on it; order them. Nothing in it needs to
  *    start at zero: each call rewrites the counts it reads, and the one word

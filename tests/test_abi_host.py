@@ -129,15 +129,36 @@ def test_sizes_near_int64_limits_are_refused_before_any_device_call(ep):
     assert lib.ep_combine(A, (1 << 31), A, A, 16, 7168, 8, A, None, None) == UNSUP  # num_recv
 
 
+def _slice_golden():
+    """Per-warp slice figures of DeepEP's intranode kernel, as the pages give
+    them (tests/golden/tma_slice_budget.txt, with its citation)."""
+    vals = {}
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "tma_slice_budget.txt")):
+        line = line.split("#", 1)[0].strip()
+        if "=" in line:
+            k, v = (x.strip() for x in line.split("=", 1))
+            vals[k] = int(v)
+    return vals
+
+
+def test_slice_golden_is_consistent():
+    g = _slice_golden()
+    assert g["warps"] == g["threads"] // 32
+    assert g["smem_bytes"] == g["bytes_per_warp"] * g["warps"]
+    assert g["row_bytes"] == 2 * g["hidden"] and g["half_row_bytes"] * 2 == g["row_bytes"]
+
+
 @pytest.mark.gpu
 def test_dispatch_chunk_bytes_plan(ep):
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    g = _slice_golden()
     try:
         ep.ep_set_num_sms(0)
-        # prefill rows of 14336 B: two 7168-B chunks fill the ring's stages
-        assert ep.ep_dispatch_chunk_bytes(4096, 7168, 8) == 7168
+        # prefill rows of 14336 B: the ring moves them in two chunks, the
+        # half rows of DeepEP's receive loop
+        assert ep.ep_dispatch_chunk_bytes(4096, g["hidden"], 8) == g["half_row_bytes"]
         # a decode batch is cut finer so every warp gets work, never below 512 B
         c = ep.ep_dispatch_chunk_bytes(128, 7168, 8)
         assert c % 16 == 0 and 512 <= c < 7168

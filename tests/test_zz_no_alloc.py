@@ -2,17 +2,25 @@
 allocate device memory (a serving engine whose HBM is already reserved for
 weights and KV cache; a latency-critical pipeline where cudaMalloc/cudaFree
 could synchronise the device). Its scratch is a static device array inside
-the library, so it must give exactly what ep_get_dispatch_layout gives with a
-caller-allocated workspace, call after call, while that array is reused.
+the library, reused by every call, so each call must still give exactly the
+layout the oracle gives, and exactly what ep_get_dispatch_layout gives with a
+caller-allocated workspace, call after call, whatever the previous call left
+in that array.
 
 This file is collected last so that a run stopping at its first failure has
 already run every other test; it also passes on its own in a fresh process.
 """
+import re
+import os
+
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from combine_movement_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.fixture(scope="module")
@@ -21,6 +29,14 @@ def ep():
     build.build()
     from combine_movement_gb300 import ep as mod
     return mod
+
+
+def test_binding_limit_matches_the_header(ep):
+    """The binding's copy of the scratch size is the header's #define."""
+    text = open(os.path.join(ROOT, "include", "ep.h")).read()
+    m = re.search(r"^#define\s+EP_NOALLOC_SCRATCH_BYTES\s+\(1u << (\d+)\)\s*$", text, re.M)
+    assert m is not None, "EP_NOALLOC_SCRATCH_BYTES is no longer (1u << n) in include/ep.h"
+    assert ep.EP_NOALLOC_SCRATCH_BYTES == 1 << int(m.group(1))
 
 
 def test_oversize_is_rejected_before_any_device_work(ep):
@@ -46,29 +62,45 @@ def _layout_noalloc(ep, idx, E, status):
     return counts, offsets, slot
 
 
+def _check(ep, wl: W.Workload, status, dev):
+    """One no-allocation call on `wl`'s routing table, checked against the
+    oracle's layout and against the workspace call, element by element."""
+    idx_cpu = W.make_inputs(wl).topk_idx
+    idx = idx_cpu.to(dev)
+    c_ref, o_ref, s_ref, st_ref = oracle.Oracle().layout(idx_cpu.numpy(), wl.E)
+    got = _layout_noalloc(ep, idx, wl.E, status)
+    assert ep.ep_get_status(status) == st_ref == ep.EP_OK
+    for g, r, name in zip(got, (c_ref, o_ref, s_ref), ("counts", "offsets", "slot")):
+        assert np.array_equal(g.cpu().numpy(), r), f"{wl.name}: {name} differs from the oracle"
+    want = _layout_with_workspace(ep, idx, wl.E)
+    for g, w, name in zip(got, want, ("counts", "offsets", "slot")):
+        assert torch.equal(g, w), f"{wl.name}: {name} differs from the workspace call"
+
+
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_layout_on_consecutive_calls(ep):
+def test_noalloc_matches_oracle_on_consecutive_calls(ep):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    # two different tables in a row, both large enough to use the scratch
-    # (smaller tables are laid out by one thread-block cluster, with none)
+    # Tables large enough to need scratch (smaller ones are laid out by one
+    # thread-block cluster, with none). The two launch shapes that use it,
+    # in a sequence where each call finds the previous one's contents:
+    #  - up to 128 tiles: one cooperative launch whose grid barrier keeps
+    #    its words in the scratch (16384 x 8 at E = 128 and 512: 128 tiles);
+    #  - more tiles: tile + finish launches (140000 x 8 at E = 128: 137
+    #    tiles, 70 KB of per-tile counts);
+    #  - then a cooperative call with another tile count (9000 x 8 at
+    #    E = 1024: 71 tiles), whose flag words still hold earlier targets.
+    big = W.Workload("noalloc-137-tiles", T=140000, H=8, E=128, K=8, seed=12)
+    small_coop = W.Workload("noalloc-coop-71-tiles", T=9000, H=8, E=1024, K=8, seed=13)
     cases = [W.sweep(16384, 64),
-             W.Workload("noalloc-e512", T=16384, H=64, E=512, K=8, seed=11)]
+             W.Workload("noalloc-e512", T=16384, H=64, E=512, K=8, seed=11),
+             big, small_coop, big, W.sweep(16384, 64)]
     for wl in cases:
-        assert ep.ep_layout_workspace_bytes(wl.T, wl.K, wl.E) > 0
+        assert 0 < ep.ep_layout_workspace_bytes(wl.T, wl.K, wl.E) <= ep.EP_NOALLOC_SCRATCH_BYTES
+    assert ep.ep_layout_launches(big.T, big.K, big.E) == 2
+    assert ep.ep_layout_launches(small_coop.T, small_coop.K, small_coop.E) == 1
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     for wl in cases:
-        idx = W.make_inputs(wl).topk_idx.to(dev)
-        want = _layout_with_workspace(ep, idx, wl.E)
-        got = _layout_noalloc(ep, idx, wl.E, status)
-        assert ep.ep_get_status(status) == ep.EP_OK
-        for g, w, name in zip(got, want, ("counts", "offsets", "slot")):
-            assert np.array_equal(g.cpu().numpy(), w.cpu().numpy()), f"{wl.name}: {name}"
-    # and the first table again, after the second left its counts in the array
-    idx = W.make_inputs(cases[0]).topk_idx.to(dev)
-    want = _layout_with_workspace(ep, idx, cases[0].E)
-    got = _layout_noalloc(ep, idx, cases[0].E, status)
-    for g, w in zip(got, want):
-        assert torch.equal(g, w)
+        _check(ep, wl, status, dev)
