@@ -270,10 +270,36 @@ def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch
             e[3].record(stream)
         end2.record(stream)
         torch.cuda.synchronize()
+        # K steps of dispatch + combine alone (the layout of the last pass
+        # still in place): the step's cost without the layout
+        start3 = torch.cuda.Event(enable_timing=True)
+        end3 = torch.cuda.Event(enable_timing=True)
+        start3.record(stream)
+        for _ in range(steps):
+            step.dispatch(step.b, stream)
+            step.combine(step.b, stream)
+        end3.record(stream)
+        # K launches of each copy kernel back to back, events only around the
+        # loop: its average launch duration (the next launch's start hides
+        # behind the previous one's end, as it does between the kernels of
+        # the step; an event between two kernels does not let it)
+        b2b = {}
+        for name, fn in (("dispatch", step.dispatch), ("combine", step.combine)):
+            fn(step.b, stream)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                fn(step.b, stream)
+            e1.record(stream)
+            b2b[name] = (e0, e1)
+        torch.cuda.synchronize()
     lay = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
     dis = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
     com = [ev[i][2].elapsed_time(ev[i][3]) for i in range(steps)]
     return {"total_ms": total_ms, "total_ms_kernel_events": start2.elapsed_time(end2),
+            "dispatch_combine_total_ms": start3.elapsed_time(end3),
+            "b2b_ms": {k: e0.elapsed_time(e1) / steps for k, (e0, e1) in b2b.items()},
             "layout_ms": lay, "dispatch_ms": dis, "combine_ms": com,
             "clocks": sampler.summary() if sampler else None}
 
@@ -1302,8 +1328,17 @@ def main():
             "step_gbs": (moved + ab["layout"]) / (ms * 1e-3) / 1e9,
             "step_frac": (moved + ab["layout"]) / (ms * 1e-3) / 1e9 / peak,
             "dispatch_us": 1e3 * d, "combine_us": 1e3 * c, "layout_us": 1e3 * lay,
+            # what the layout adds to the step: the step minus dispatch +
+            # combine alone (both K steps, no events between the kernels)
+            "layout_in_step_us": 1e3 * (run["total_ms"] - run["dispatch_combine_total_ms"])
+                                 / args.steps,
             "dispatch_gbs": ab["dispatch"] / (d * 1e-3) / 1e9,
             "combine_gbs": ab["combine"] / (c * 1e-3) / 1e9,
+            # each copy kernel's average launch duration over K launches back
+            # to back, and its bandwidth from that
+            "b2b_us": {k: 1e3 * v for k, v in run["b2b_ms"].items()},
+            "dispatch_gbs_b2b": ab["dispatch"] / (run["b2b_ms"]["dispatch"] * 1e-3) / 1e9,
+            "combine_gbs_b2b": ab["combine"] / (run["b2b_ms"]["combine"] * 1e-3) / 1e9,
             "us_median_p10_p90": {k: spread(run[f"{k}_ms"])
                                   for k in ("layout", "dispatch", "combine")},
         }
@@ -1320,7 +1355,7 @@ def main():
     s_all = summarize(main_run, sms_all)
     s_bud = summarize(budget_run, min(args.budget_sms, sms_all))
     dom = "dispatch" if s_all["dispatch_us"] >= s_all["combine_us"] else "combine"
-    achieved = s_all[f"{dom}_gbs"]
+    achieved = s_all[f"{dom}_gbs_b2b"]
     traffic = kernel_traffic(dom)
     e2e_ms = max_over_ranks(e2e["ms_per_step"], dist_on)
 
@@ -1361,6 +1396,11 @@ def main():
                 "bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_bytes": ab[dom],
+                "launch_us": s_all["b2b_us"][dom],
+                "timing": f"{args.steps} {dom} launches back to back between two CUDA events "
+                          "on the launching stream (the in-step figure with events around "
+                          "each kernel is hbm.all_sms." + dom + "_us)",
+                "in_step_frac": s_all[f"{dom}_gbs"] / peak,
             },
             # the same figures for both HBM-bound kernels (all SMs and the
             # second budget); the layout is latency-bound and has none

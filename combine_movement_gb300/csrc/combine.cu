@@ -27,6 +27,7 @@
 #include "combine_math.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "work_split.cuh"
 
 namespace ep {
 namespace {
@@ -47,6 +48,11 @@ struct CombineShape {
     bool slot_rows;
 };
 constexpr CombineShape combine_shape(int KT) {
+#ifdef EP_COMBINE_SHAPE_OVERRIDE
+    // measurement builds: threads * 10 + column blocks, rows by slot index,
+    // for every K <= 8
+    if (KT > 0) return {EP_COMBINE_SHAPE_OVERRIDE / 10, EP_COMBINE_SHAPE_OVERRIDE % 10, true};
+#endif
     switch (KT) {
         case 1: return {1024, 4, true};
         case 2: return {1024, 2, false};
@@ -86,8 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
     const int64_t units = a.T * n_cb;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
-    const int64_t u0 = units * gw / nw_total;
-    const int64_t u1 = units * (gw + 1) / nw_total;
+    const int64_t u0 = split_begin(units, gw, nw_total);
+    const int64_t u1 = split_begin(units, gw + 1, nw_total);
     const int K = KT > 0 ? KT : a.K;
     constexpr int KR = KT > 0 ? KT : 1;
 
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs 
     float w_lane = 0.0f;
 
     // (token, column block) of the current unit, advanced without divisions
-    int64_t t = u0 / n_cb;
+    int64_t t = div_floor(u0, n_cb);
     uint32_t cb = static_cast<uint32_t>(u0 - t * n_cb);
     for (int64_t u = u0; u < u1; ++u) {
         const uint32_t col0 = cb * kUnitBytes + lane * 16u;

@@ -29,6 +29,7 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "routing.cuh"
+#include "work_split.cuh"
 
 namespace ep {
 namespace {
@@ -59,23 +60,39 @@ __host__ __device__ constexpr uint32_t barrier_region(int stages, int warps) {
     return (8u * stages * warps + 127u) & ~127u;
 }
 
+// Entries [i0, i1) of the routing table: the (token, k) cells of the tokens
+// a fused-kernel CTA moves (the union of its warps' unit ranges).
+struct CtaEntries {
+    int64_t i0, i1;
+};
+__device__ __forceinline__ CtaEntries cta_entries(const DispatchArgs& a, int64_t units,
+                                                  int64_t nw_total) {
+    const int nwarps = blockDim.x >> 5;
+    const int64_t cu0 = split_begin(units, static_cast<int64_t>(blockIdx.x) * nwarps, nw_total);
+    const int64_t cu1 = split_begin(units, static_cast<int64_t>(blockIdx.x + 1) * nwarps, nw_total);
+    const int64_t t0 = div_floor(cu0, a.n_chunks);
+    const int64_t t1 = cu1 > cu0 ? div_floor(cu1 - 1, a.n_chunks) + 1 : t0;
+    return {t0 * a.K, t1 * a.K};
+}
+
 // Layout prologue of the fused kernel (see dispatch_kernel). All threads of
 // the CTA take part; ends with a block barrier after which the slots of the
-// CTA's tokens are in global memory.
-__device__ __noinline__ void fused_layout(const DispatchArgs& a, const FusedLayoutArgs& f,
-                                          uint8_t* smem, int64_t units, int64_t nw_total) {
+// CTA's entries are in global memory and, when f.own_off != 0, in shared
+// memory too (own_slot[i - i0]). `prefetch()` runs once, right after the
+// first routing-table loads are issued: the ring's first row loads then
+// queue behind them instead of delaying them.
+template <class Prefetch>
+__device__ __forceinline__ void fused_layout(const DispatchArgs& a, const FusedLayoutArgs& f,
+                                          uint8_t* smem, CtaEntries own, Prefetch prefetch) {
     const int E = f.E;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
     int32_t* total = reinterpret_cast<int32_t*>(smem + f.hist_off);
     int32_t* run = total + E;
+    int16_t* own_key = reinterpret_cast<int16_t*>(smem + f.own_off);
+    int32_t* own_slot = reinterpret_cast<int32_t*>(smem + f.own_off + kFusedOwnCap * sizeof(int16_t));
+    const bool keep = f.own_off != 0;
     const int64_t N = a.T * a.K;
-    // this CTA's tokens: the union of its warps' unit ranges
-    const int64_t cu0 = units * (static_cast<int64_t>(blockIdx.x) * nwarps) / nw_total;
-    const int64_t cu1 = units * (static_cast<int64_t>(blockIdx.x + 1) * nwarps) / nw_total;
-    const int64_t t0 = cu0 / a.n_chunks;
-    const int64_t t1 = cu1 > cu0 ? (cu1 - 1) / a.n_chunks + 1 : t0;
-    const int64_t i0 = t0 * a.K, i1 = t1 * a.K;
+    const int64_t i0 = own.i0, i1 = own.i1;
 
     for (int e = threadIdx.x; e < E; e += blockDim.x) total[e] = run[e] = 0;
     __syncthreads();
@@ -88,6 +105,8 @@ __device__ __noinline__ void fused_layout(const DispatchArgs& a, const FusedLayo
         } else if (v != -1) {
             bad = true;
         }
+        // the CTA's own entries are ranked from shared memory below
+        if (keep && i >= i0 && i < i1) own_key[i - i0] = static_cast<int16_t>(e);
     };
     // 16-byte loads (two ids each), 16 in flight per thread; an 8-byte-
     // aligned first id and an odd last id are read on their own.
@@ -95,12 +114,17 @@ __device__ __noinline__ void fused_layout(const DispatchArgs& a, const FusedLayo
     const int64_t pairs = N > head ? (N - head) / 2 : 0;
     const longlong2* pv = reinterpret_cast<const longlong2*>(f.idx + head);
     constexpr int kBatch = 16;
+    bool prefetched = false;
     for (int64_t b0 = threadIdx.x; b0 < pairs; b0 += static_cast<int64_t>(blockDim.x) * kBatch) {
         longlong2 v[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int64_t q = b0 + static_cast<int64_t>(u) * blockDim.x;
             v[u] = q < pairs ? __ldg(pv + q) : make_longlong2(-1, -1);
+        }
+        if (!prefetched) {
+            prefetch();
+            prefetched = true;
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
@@ -111,6 +135,7 @@ __device__ __noinline__ void fused_layout(const DispatchArgs& a, const FusedLayo
             }
         }
     }
+    if (!prefetched) prefetch();
     if (threadIdx.x == 0) {
         if (head && N > 0) count(0, __ldg(f.idx));
         const int64_t last = head + 2 * pairs;
@@ -135,8 +160,9 @@ __device__ __noinline__ void fused_layout(const DispatchArgs& a, const FusedLayo
     if (blockIdx.x == 0 && threadIdx.x == 0) f.offsets[E] = static_cast<int32_t>(all);
     __syncthreads();
     if (warp == 0) {
-        // 8 rounds of ids are loaded together (one memory latency per 256
-        // entries), then ranked round by round in entry order.
+        // 8 rounds of ids are read together (from shared memory when kept
+        // there, else one global-memory latency per 256 entries), then
+        // ranked round by round in entry order.
         const int kbits = key_bits_for(E);
         constexpr int kRounds = 8;
         for (int64_t b0 = i0; b0 < i1; b0 += 32 * kRounds) {
@@ -144,15 +170,18 @@ __device__ __noinline__ void fused_layout(const DispatchArgs& a, const FusedLayo
 #pragma unroll
             for (int r = 0; r < kRounds; ++r) {
                 const int64_t i = b0 + r * 32 + lane;
-                key[r] = i < i1 ? expert_key(__ldg(f.idx + i), E) : -1;
+                key[r] = i >= i1 ? -1 : keep ? own_key[i - i0] : expert_key(__ldg(f.idx + i), E);
             }
 #pragma unroll
             for (int r = 0; r < kRounds; ++r) {
                 const int64_t i = b0 + r * 32 + lane;
                 if (b0 + r * 32 >= i1) break;
                 const uint32_t peers = peers_of(key[r], kbits);
-                if (i < i1)
-                    f.slot[i] = key[r] >= 0 ? run[key[r]] + __popc(peers & lanemask_lt()) : -1;
+                if (i < i1) {
+                    const int32_t sl = key[r] >= 0 ? run[key[r]] + __popc(peers & lanemask_lt()) : -1;
+                    f.slot[i] = sl;
+                    if (keep) own_slot[i - i0] = sl;
+                }
                 __syncwarp();
                 if (key[r] >= 0 && lane == __ffs(peers) - 1) run[key[r]] += __popc(peers);
                 __syncwarp();
@@ -203,8 +232,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
-    const int64_t u0 = units * gw / nw_total;
-    const int64_t n = units * (gw + 1) / nw_total - u0;
+    const int64_t u0 = split_begin(units, gw, nw_total);
+    const int64_t n = split_begin(units, gw + 1, nw_total) - u0;
 
     // L2 policies: x is read once (evict first); the receive rows are
     // written once and next read by the experts (normal).
@@ -219,12 +248,19 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     const uint64_t pol_load = policy_evict_first();
 #endif
 
-    // Bulk-load local unit j (token, chunk) into its ring stage.
+    // Bulk-load the next unit (token lt, chunk lc) into the stage of local
+    // unit j (units are loaded in order, so (lt, lc) just advances).
+    int64_t lt = div_floor(u0, a.n_chunks);
+    uint32_t lc = static_cast<uint32_t>(u0 - lt * a.n_chunks);
     auto issue_load = [&](int64_t j) {
+        const int64_t t = lt;
+        const uint32_t c = lc;
+        if (++lc == a.n_chunks) {
+            lc = 0;
+            ++lt;
+        }
         if (!leader) return;
-        const int64_t u = u0 + j;
-        const int64_t t = u / a.n_chunks;
-        const uint32_t off = static_cast<uint32_t>(u - t * a.n_chunks) * a.chunk_bytes;
+        const uint32_t off = c * a.chunk_bytes;
         const uint32_t bytes = min(a.chunk_bytes, a.row_bytes - off);
         const int s = static_cast<int>(j % NS);
         const uint32_t bar = bar0 + 8u * s;
@@ -233,11 +269,20 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
                   a.x + t * static_cast<int64_t>(a.row_bytes) + off, bytes, bar, pol_load);
     };
 
+    // The fused kernel's entries: the CTA's slots stay in shared memory
+    // (own_slot) when f.own_off != 0.
+    const CtaEntries own = FUSED ? cta_entries(a, units, nw_total) : CtaEntries{0, 0};
+    const int32_t* own_slot =
+        reinterpret_cast<const int32_t*>(smem + f.own_off + kFusedOwnCap * sizeof(int16_t));
+
     // Lanes k < K hold slot[t][k] (and topk_w[t][k]) of the current token and
     // of the next one, loaded a token ahead.
     auto load_slot = [&](int64_t t) -> int32_t {
         if (t >= a.T || lane >= a.K) return -1;
-        return FUSED ? ld_plain_s32(a.slot + t * a.K + lane) : __ldg(a.slot + t * a.K + lane);
+        if (!FUSED) return __ldg(a.slot + t * a.K + lane);
+        const int64_t i = t * a.K + lane;
+        if (f.own_off != 0) return (i >= own.i0 && i < own.i1) ? own_slot[i - own.i0] : -1;
+        return ld_plain_s32(a.slot + i);
     };
     auto load_w = [&](int64_t t) -> float {
         return (a.topk_w != nullptr && t < a.T && lane < a.K) ? __ldg(a.topk_w + t * a.K + lane)
@@ -245,20 +290,30 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     };
 
     // The rows of x do not depend on the layout, so the first loads go out
-    // before the fused kernel computes it (every thread of the CTA then
-    // takes part in that, whatever its own share of units).
-    for (int64_t j = 0; j < P && j < n; ++j) issue_load(j);
-    if (FUSED) fused_layout(a, f, smem, units, nw_total);
+    // before the fused kernel computes it, right behind its routing-table
+    // loads (every thread of the CTA then takes part in the layout, whatever
+    // its own share of units).
+    auto first_loads = [&]() {
+        for (int64_t j = 0; j < P && j < n; ++j) issue_load(j);
+    };
+    if (FUSED)
+        fused_layout(a, f, smem, own, first_loads);
+    else
+        first_loads();
     if (n <= 0) return;
 
-    int64_t tok = u0 / a.n_chunks;
+    int64_t tok = div_floor(u0, a.n_chunks);
     int32_t s_cur = load_slot(tok), s_next = load_slot(tok + 1);
     float w_cur = load_w(tok), w_next = load_w(tok + 1);
 
-    for (int64_t j = 0; j < n; ++j) {
-        const int64_t u = u0 + j;
-        const int64_t t = u / a.n_chunks;
-        const uint32_t c = static_cast<uint32_t>(u - t * a.n_chunks);
+    // (token, chunk) of local unit j, advanced without divisions
+    int64_t t = tok;
+    uint32_t c = static_cast<uint32_t>(u0 - tok * a.n_chunks);
+    for (int64_t j = 0; j < n; ++j, ++c) {
+        if (c == a.n_chunks) {
+            c = 0;
+            ++t;
+        }
         if (t != tok) {
             tok = t;
             s_cur = s_next;
@@ -307,8 +362,12 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
             if (a.recv_src != nullptr) a.recv_src[s_cur] = static_cast<int32_t>(t * a.K + lane);
         }
     }
-    // Shared memory must outlive every bulk store that reads it.
-    if (leader) bulk_wait<0>();
+    // Shared memory must outlive every bulk store that reads it: wait until
+    // they have all read their stage. Their writes to global memory need no
+    // wait here (they complete with the grid, before any later kernel on the
+    // stream, or one waiting on this grid's completion, can see the grid
+    // done), so the CTA leaves without the write acknowledgements' latency.
+    if (leader) bulk_wait_read<0>();
 }
 
 // ---- ablation: the same copy through the load/store units ---------------------
@@ -342,7 +401,7 @@ __global__ void __launch_bounds__(kLsuThreads, 1) dispatch_lsu_kernel(const Disp
     const int64_t units = a.T * n_cb;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
-    const int64_t u0 = units * gw / nw_total, u1 = units * (gw + 1) / nw_total;
+    const int64_t u0 = split_begin(units, gw, nw_total), u1 = split_begin(units, gw + 1, nw_total);
     int64_t tok = -1;
     int32_t s_lane = -1;
     for (int64_t u = u0; u < u1; ++u) {
@@ -450,15 +509,27 @@ cudaError_t launch_layout_dispatch(const DispatchArgs& a, FusedLayoutArgs f, int
     const size_t ring = static_cast<size_t>(barrier_region(kStages, kDispatchWarps)) +
                         static_cast<size_t>(kDispatchWarps) * kStages * a.stage_bytes;
     f.hist_off = static_cast<uint32_t>(ring);
-    size_t smem = ring + 2 * sizeof(int32_t) * static_cast<size_t>(f.E);
+    const size_t hist_end = ring + 2 * sizeof(int32_t) * static_cast<size_t>(f.E);
+    const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
+    const int64_t ctas_needed = (units + kDispatchWarps - 1) / kDispatchWarps;
+    const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
+    // the most entries any CTA lays out (same split as the kernel's)
+    int64_t most = 0;
+    const int64_t nw_total = static_cast<int64_t>(grid > 0 ? grid : 1) * kDispatchWarps;
+    for (int b = 0; b < grid; ++b) {
+        const int64_t cu0 = units * (static_cast<int64_t>(b) * kDispatchWarps) / nw_total;
+        const int64_t cu1 = units * (static_cast<int64_t>(b + 1) * kDispatchWarps) / nw_total;
+        const int64_t t0 = cu0 / a.n_chunks;
+        const int64_t t1 = cu1 > cu0 ? (cu1 - 1) / a.n_chunks + 1 : t0;
+        if ((t1 - t0) * a.K > most) most = (t1 - t0) * a.K;
+    }
+    f.own_off = most <= kFusedOwnCap ? static_cast<uint32_t>((hist_end + 15) & ~size_t{15}) : 0u;
+    size_t smem = ((hist_end + 15) & ~size_t{15}) + kFusedOwnBytes;
     if (smem < kExclusiveSmem) smem = kExclusiveSmem;
     auto kern = dispatch_kernel<kStages, kPrefetch, true>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
-    const int64_t ctas_needed = (units + kDispatchWarps - 1) / kDispatchWarps;
-    const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
     return launch_dependent(kern, grid > 0 ? grid : 1, kDispatchWarps * 32, smem, stream, a, f);
 }
 

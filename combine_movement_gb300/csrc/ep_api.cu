@@ -280,7 +280,8 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
     int sm_count = 0, smem_optin = 0;
     if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
     ep::DispatchArgs a{};
-    const size_t hist = 2 * sizeof(int32_t) * static_cast<size_t>(E);
+    // histograms, 16-byte alignment, the CTA's own keys and slots
+    const size_t hist = 2 * sizeof(int32_t) * static_cast<size_t>(E) + 16 + ep::kFusedOwnBytes;
     st = plan_dispatch(&a, x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src, status,
                        smem_optin, hist, sms_in_effect(sm_count), true);
     if (st != EP_OK) return st;

@@ -90,7 +90,14 @@ struct FusedLayoutArgs {
     int32_t* offsets;
     int32_t* slot;      // the same array as DispatchArgs::slot, written by the kernel
     uint32_t hist_off;  // shared-memory byte offset of its 2*E histogram words
+    // Shared-memory byte offset of the CTA's own entries (kFusedOwnCap
+    // int16 expert keys, then kFusedOwnCap int32 slots), or 0 when some CTA
+    // has more entries than that (its slots then go through global memory).
+    uint32_t own_off;
 };
+// Routing entries a fused-kernel CTA keeps in shared memory.
+constexpr int kFusedOwnCap = 1024;
+constexpr size_t kFusedOwnBytes = kFusedOwnCap * (sizeof(int16_t) + sizeof(int32_t));
 
 cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, int smem_optin,
                             cudaStream_t stream);

@@ -135,9 +135,10 @@ EP_API int ep_layout_launches(int64_t T, int K, int E);
 EP_API int64_t ep_dispatch_chunk_bytes(int64_t T, int64_t H, int K);
 
 /* Stages of the per-warp shared-memory ring ep_dispatch uses at the current
- * SM budget and launch-overlap mode: 3 while launches overlap (so a dispatch
- * CTA fits beside a layout CTA on one SM), else 4. For measurements that
- * model the ring. */
+ * SM budget and launch-overlap mode: 3 while launches overlap (a dispatch CTA
+ * then needs less shared memory, so its SM keeps a larger L1 share; measured
+ * faster with the kernels overlapping), else 4. For measurements that model
+ * the ring. */
 EP_API int ep_dispatch_ring_stages(void);
 
 /* Layout (per-expert histogram, exclusive prefix sums and per-(token,k)
