@@ -471,10 +471,13 @@ def spread(ms: list) -> list:
 
 
 def time_call(fn, reps: int, flush=None) -> float:
-    """Median microseconds of fn() on the current stream (CUDA events). The
-    GPU is kept busy (L2 flush, or a ~100 us spin, longer than the host takes
-    to enqueue a step through the Python binding) while the host enqueues
-    the call, so host launch overhead is not counted."""
+    """Microseconds of fn() on the current stream (CUDA events): the mean of
+    the middle 80 % of `reps` calls. Event timestamps on this GPU are
+    quantised near 1 us, so a median would be too; the trimmed mean of calls
+    that jitter across the quanta is not. The GPU is kept busy (L2 flush,
+    or a ~100 us spin, longer than the host takes to enqueue a step through
+    the Python binding) while the host enqueues the call, so host launch
+    overhead is not counted."""
     ts = []
     for i in range(reps + 3):
         if flush is not None:
@@ -489,7 +492,9 @@ def time_call(fn, reps: int, flush=None) -> float:
         torch.cuda.synchronize()
         if i >= 3:
             ts.append(a.elapsed_time(b) * 1e3)
-    return statistics.median(ts)
+    ts.sort()
+    cut = len(ts) // 10
+    return statistics.mean(ts[cut:len(ts) - cut])
 
 
 def empty_launch_us(reps: int = 200) -> float:
@@ -939,7 +944,7 @@ def run_pipeline_model(ep, dev, wl: W.Workload, budgets=(0, 24, 16)) -> None:
     stage alone and its store stage alone (same ring shape, chunk, units per
     warp; probes above), take per-unit stage times t = stage time / N with
     N = units per warp, and print the closed form, the serial sum and the
-    measured dispatch time (all cold L2, medians). One JSON line per budget."""
+    measured dispatch time (all cold L2, time_call's trimmed means). One JSON line per budget."""
     import ctypes
     L = _probe_lib()
     step = Step(ep, W.make_inputs(wl), dev)
@@ -1190,6 +1195,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="deepseek-v3-prefill", choices=sorted(W.BY_NAME))
     ap.add_argument("--budget-sms", type=int, default=24, help="second SM budget to report")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (same shapes and seed; for "
+                         "profiling captures on a smaller case of the same kernels)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: the T x H x SM-budget sweep, one JSON line each")
@@ -1223,6 +1231,9 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("gloo")
     wl = W.BY_NAME[args.workload]
+    if args.tokens > 0:
+        import dataclasses
+        wl = dataclasses.replace(wl, T=args.tokens)
 
     if args.impl == "reference":
         run_reference(args, wl, rank)
