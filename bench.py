@@ -736,7 +736,8 @@ def run_workloads(ep, dev, budget: int, steps: int, warmup: int) -> None:
 
 def run_sweep(ep, dev, budgets) -> None:
     """SM-budget and size sweep: one JSON line per (T, H, budget) with each
-    kernel's median time (cold L2) and GB/s against the HBM peak."""
+    kernel's time (time_call's trimmed mean, cold L2) and GB/s against the
+    HBM peak."""
     peak, _ = peak_hbm()
     flush = _Flusher(dev)
     sms_all = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -944,7 +945,8 @@ def run_pipeline_model(ep, dev, wl: W.Workload, budgets=(0, 24, 16)) -> None:
     stage alone and its store stage alone (same ring shape, chunk, units per
     warp; probes above), take per-unit stage times t = stage time / N with
     N = units per warp, and print the closed form, the serial sum and the
-    measured dispatch time (all cold L2, time_call's trimmed means). One JSON line per budget."""
+    measured dispatch time (all cold L2, time_call's trimmed means). One
+    JSON line per budget."""
     import ctypes
     L = _probe_lib()
     step = Step(ep, W.make_inputs(wl), dev)
