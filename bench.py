@@ -630,6 +630,21 @@ def decode_latency(ep, dev, budgets=(16, 24, 0), ceilings: dict | None = None) -
                           "combine": round(k_com, 2)},
             "kernel_net_us": {k: round(v, 2) for k, v in net.items()},
         }
+        if 0 < b < sms_all:
+            # the same step in an SM partition of b SMs (ep_sm_partition): the
+            # hardware keeps its kernels on those SMs, and the default policy
+            # lets their launches overlap
+            try:
+                h, _, n_part, _ = ep.ep_sm_partition(b)
+                ps = torch.cuda.ExternalStream(h, device=dev)
+                with torch.cuda.stream(ps):
+                    pw = time_call(lambda: step.run(step.b), 200)
+                    pf = time_call(lambda: step.run_fused(step.b), 200)
+                    pb = back_to_back(lambda: step.run(step.b))
+                entry["partition"] = {"sms": n_part, "warm_us": round(pw, 2),
+                                      "fused_warm_us": round(pf, 2), "back_to_back_us": round(pb, 2)}
+            except Exception as e:  # noqa: BLE001 - reported in the line
+                entry["partition"] = {"unavailable": str(e)[:200]}
         c = (ceilings or {}).get(n)
         if c:
             w_cap, r_cap = c["write_l2_gbs"], c["read_l2_gbs"]
@@ -1133,10 +1148,21 @@ def run_overlap(ep, dev, wl: W.Workload, budgets=(16, 24, 48), steps: int = 60) 
             step.dispatch(step.b, s_move)
             step.combine(step.b, s_move)
 
-    for n, mode in [(n, m) for n in budgets for m in (0, 1)]:
+    plain = (s_move, s_comp)
+    cases = [(n, m, False) for n in budgets for m in (0, 1)] + [(n, 0, True) for n in budgets]
+    for n, mode, part in cases:
         ep.ep_set_num_sms(n)
         ep.ep_set_launch_overlap(mode)  # 0: library default (no overlap below the full budget)
         grid = sms - n
+        s_move, s_comp = plain
+        if part:
+            # movement in an SM partition of n SMs, the ALU kernel in the
+            # partition of the other SMs (the default policy overlaps
+            # launches in a partition)
+            h, hr, n_part, n_rest = ep.ep_sm_partition(n)
+            s_move = torch.cuda.ExternalStream(h, device=dev)
+            s_comp = torch.cuda.ExternalStream(hr, device=dev)
+            grid = n_rest
         with torch.cuda.stream(s_move):
             movement(3)
         torch.cuda.synchronize(dev)
@@ -1175,7 +1201,9 @@ def run_overlap(ep, dev, wl: W.Workload, budgets=(16, 24, 48), steps: int = 60) 
         print(json.dumps({
             "workload": wl.name, "step": "layout+dispatch+combine" if small else "dispatch+combine",
             "num_sms_movement": n, "num_sms_alu": grid, "steps": steps,
-            "launch_overlap": "auto (off below the full budget)" if mode == 0 else "forced on",
+            "launch_overlap": ("auto (on in a partition)" if part else
+                               "auto (off below the full budget)") if mode == 0 else "forced on",
+            "sm_partition": part,
             "movement_ms_per_step_alone": round(move_ms / steps, 4),
             "movement_ms_per_step_overlapped": round(a0.elapsed_time(a1) / steps, 4),
             "alu_ms_alone": round(comp_ms, 3), "alu_ms_overlapped": round(c0.elapsed_time(c1), 3),
@@ -1310,6 +1338,16 @@ def main():
         return
     ep.ep_set_num_sms(args.budget_sms)
     budget_run = time_steps(step, args.steps, args.warmup, dist_on, stream)
+    # the same budget as an SM partition (ep_sm_partition): its kernels stay
+    # on those SMs and their launches may overlap
+    part_run, part_sms = None, 0
+    if 0 < args.budget_sms < sms_all:
+        try:
+            h, _, part_sms, _ = ep.ep_sm_partition(args.budget_sms)
+            part_run = time_steps(step, args.steps, args.warmup, dist_on,
+                                  torch.cuda.ExternalStream(h, device=dev))
+        except Exception as e:  # noqa: BLE001 - reported in the line
+            log(f"SM partition unavailable: {e}")
     ep.ep_set_num_sms(0)
     fused_run = time_fused_steps(step, args.steps, args.warmup, dist_on, stream)
     ep.ep_set_num_sms(args.budget_sms)
@@ -1401,6 +1439,8 @@ def main():
                 "fused_all_sms": summarize_fused(fused_run, sms_all),
                 f"fused_sms_{args.budget_sms}": summarize_fused(fused_budget,
                                                                 min(args.budget_sms, sms_all)),
+                f"partition_sms_{args.budget_sms}": (summarize(part_run, part_sms)
+                                                     if part_run else None),
                 "peak_gbs": peak,
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_step": ab,

@@ -487,8 +487,8 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, int smem_optin,
     return launch_ring<kStages>(a, num_sms, stream);
 }
 
-int dispatch_ring_stages(bool fused) {
-    return (!fused && launch_overlap_allowed()) ? kSharedStages : kStages;
+int dispatch_ring_stages(bool fused, cudaStream_t stream) {
+    return (!fused && launch_overlap_allowed(stream)) ? kSharedStages : kStages;
 }
 
 // Stage size the host plans rows with: the per-warp slice (what is left of

@@ -60,16 +60,26 @@ int sms_in_effect(int sm_count) {
     return (b <= 0 || b > sm_count) ? sm_count : b;
 }
 
+// SMs a copy kernel launched into `stream` uses: the budget, and no more
+// than the SMs of the partition the stream belongs to, if any.
+int sms_for_stream(int sm_count, cudaStream_t stream) {
+    const int n = sms_in_effect(sm_count);
+    const int part = ep::partition_sms(stream);
+    return (part > 0 && part < n) ? part : n;
+}
+
 }  // namespace
 
 namespace ep {
-// Programmatic dependent launch only while the SM budget covers the whole
-// current device (see launch_dependent).
-bool launch_overlap_allowed() {
+// Programmatic dependent launch (see launch_dependent): in the default mode
+// while the SM budget covers the whole current device, or for a launch into
+// an SM-partition stream.
+bool launch_overlap_allowed(cudaStream_t stream) {
     if (!EP_PDL) return false;
     const int mode = g_overlap_mode.load(std::memory_order_relaxed);
     if (mode == 1) return true;
     if (mode == 2) return false;
+    if (partition_sms(stream) > 0) return true;
     int c = 0, s = 0;
     if (!device_limits(&c, &s)) return false;
     return sms_in_effect(c) == c;
@@ -133,7 +143,8 @@ ep_status_t check_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const
 ep_status_t plan_dispatch(ep::DispatchArgs* a, const uint16_t* x, int64_t T, int64_t H, int K,
                           const int32_t* slot, const float* topk_w, int64_t num_recv,
                           uint16_t* recv_x, float* recv_w, int32_t* recv_src, int32_t* status,
-                          int smem_optin, size_t reserve, int num_sms, bool fused) {
+                          int smem_optin, size_t reserve, int num_sms, bool fused,
+                          cudaStream_t stream) {
     a->x = reinterpret_cast<const uint8_t*>(x);
     a->T = T;
     a->row_bytes = static_cast<uint32_t>(H * 2);
@@ -145,7 +156,7 @@ ep_status_t plan_dispatch(ep::DispatchArgs* a, const uint16_t* x, int64_t T, int
     a->recv_w = recv_w;
     a->recv_src = recv_src;
     a->status = status;
-    a->ring_stages = ep::dispatch_ring_stages(fused);
+    a->ring_stages = ep::dispatch_ring_stages(fused, stream);
     uint32_t cap = ep::dispatch_stage_capacity(smem_optin, reserve, a->ring_stages);
     if (cap < 16) return EP_ERR_UNSUPPORTED;
 #ifdef EP_DISPATCH_MAX_CHUNK
@@ -218,12 +229,12 @@ int64_t ep_dispatch_chunk_bytes(int64_t T, int64_t H, int K) {
     if (!device_limits(&sm_count, &smem_optin)) return -1;
     ep::DispatchArgs a{};
     if (plan_dispatch(&a, nullptr, T, H, K, nullptr, nullptr, 0, nullptr, nullptr, nullptr,
-                      nullptr, smem_optin, 0, sms_in_effect(sm_count), false) != EP_OK)
+                      nullptr, smem_optin, 0, sms_in_effect(sm_count), false, nullptr) != EP_OK)
         return -1;
     return a.chunk_bytes;
 }
 
-int ep_dispatch_ring_stages(void) { return ep::dispatch_ring_stages(false); }
+int ep_dispatch_ring_stages(void) { return ep::dispatch_ring_stages(false, nullptr); }
 
 ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, int E,
                                    int32_t* counts, int32_t* offsets, int32_t* slot,
@@ -256,12 +267,13 @@ ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const in
     if (st != EP_OK || T == 0) return st;
     int sm_count = 0, smem_optin = 0;
     if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int n = sms_for_stream(sm_count, s);
     ep::DispatchArgs a{};
     st = plan_dispatch(&a, x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src, status,
-                       smem_optin, 0, sms_in_effect(sm_count), false);
+                       smem_optin, 0, n, false, s);
     if (st != EP_OK) return st;
-    return from_cuda(ep::launch_dispatch(a, sms_in_effect(sm_count), smem_optin,
-                                         static_cast<cudaStream_t>(stream)));
+    return from_cuda(ep::launch_dispatch(a, n, smem_optin, s));
 }
 
 ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64_t T, int64_t H,
@@ -279,11 +291,13 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
     if (st != EP_OK) return st;
     int sm_count = 0, smem_optin = 0;
     if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int n = sms_for_stream(sm_count, s);
     ep::DispatchArgs a{};
     // histograms, 16-byte alignment, the CTA's own keys and slots
     const size_t hist = 2 * sizeof(int32_t) * static_cast<size_t>(E) + 16 + ep::kFusedOwnBytes;
     st = plan_dispatch(&a, x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src, status,
-                       smem_optin, hist, sms_in_effect(sm_count), true);
+                       smem_optin, hist, n, true, s);
     if (st != EP_OK) return st;
     ep::FusedLayoutArgs f{};
     f.idx = topk_idx;
@@ -291,8 +305,7 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
     f.counts = counts;
     f.offsets = offsets;
     f.slot = slot;
-    return from_cuda(ep::launch_layout_dispatch(a, f, sms_in_effect(sm_count),
-                                                static_cast<cudaStream_t>(stream)));
+    return from_cuda(ep::launch_layout_dispatch(a, f, n, s));
 }
 
 ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv, const int32_t* slot,
@@ -321,7 +334,7 @@ ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv, const int32
     a.K = K;
     a.y = reinterpret_cast<uint8_t*>(y);
     a.status = status;
-    const int n = sms_in_effect(sm_count);
+    const int n = sms_for_stream(sm_count, static_cast<cudaStream_t>(stream));
     if (use_combine_tma(K, n))
         return from_cuda(ep::launch_combine_tma(a, n, smem_optin, static_cast<cudaStream_t>(stream)));
     return from_cuda(ep::launch_combine(a, n, static_cast<cudaStream_t>(stream)));

@@ -111,9 +111,9 @@ cudaError_t launch_layout_dispatch(const DispatchArgs& a, FusedLayoutArgs f, int
 // whose per-block shared-memory opt-in limit is `smem_optin`, after
 // reserving `reserve` bytes for other shared data.
 uint32_t dispatch_stage_capacity(int smem_optin, size_t reserve, int stages);
-// Stages of the dispatch ring the next launch will use (fused: the
-// layout-plus-dispatch kernel); plan rows with the same number.
-int dispatch_ring_stages(bool fused);
+// Stages of the dispatch ring the next launch into `stream` will use
+// (fused: the layout-plus-dispatch kernel); plan rows with the same number.
+int dispatch_ring_stages(bool fused, cudaStream_t stream);
 
 // Warps per dispatch CTA.
 int dispatch_warps();
@@ -146,15 +146,23 @@ cudaError_t launch_combine_tma(const CombineArgs& a, int num_sms, int smem_optin
 // before touching global memory, so the launch latency overlaps the previous
 // kernel's tail. On the DeepSeek-V3 prefill step this saves ~2 us of ~193;
 // on the decode step (T=128) 3-5 us of ~21-41.
-// It is used only while the SM budget covers the whole GPU
-// (launch_overlap_allowed()). A smaller budget means the GPU is shared with
-// concurrent work, and there the early launches measured slower: dispatch +
-// combine on 24 SMs next to an ALU-bound kernel on the other 128 took 24 %
-// longer with them than without, and 0 % longer without them.
+// By default it is used only while the SM budget covers the whole GPU, or
+// for launches into an SM-partition stream (launch_overlap_allowed). A
+// smaller budget on an ordinary stream means the GPU is shared with
+// concurrent work on SMs the hardware picks, and there an early-launched
+// kernel may land on an SM the foreign work keeps busy: beside an ALU-bound
+// kernel on the other SMs, the decode step on 24 SMs took twice as long with
+// early launches, and prefill dispatch + combine 3-6 % longer. A partition
+// stream's kernels run only on the partition's SMs, where nothing foreign
+// can sit.
 #ifndef EP_PDL
 #define EP_PDL 1
 #endif
-bool launch_overlap_allowed();
+bool launch_overlap_allowed(cudaStream_t stream);
+
+// SMs of the partition `stream` belongs to (ep_sm_partition), or 0 for any
+// other stream.
+int partition_sms(cudaStream_t stream);
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent(void (*kernel)(KArgs...), int grid, int block, size_t smem,
@@ -166,7 +174,7 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), int grid, int block, size
     cfg.stream = stream;
     cudaLaunchAttribute attr{};
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = launch_overlap_allowed() ? 1 : 0;
+    attr.val.programmaticStreamSerializationAllowed = launch_overlap_allowed(stream) ? 1 : 0;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);

@@ -702,7 +702,7 @@ cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,
         attr[0].val.clusterDim.z = 1;
         // as launch_dependent: may start while the previous kernel finishes
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[1].val.programmaticStreamSerializationAllowed = launch_overlap_allowed() ? 1 : 0;
+        attr[1].val.programmaticStreamSerializationAllowed = launch_overlap_allowed(stream) ? 1 : 0;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, idx, N, E, p.rounds, counts, offsets,

@@ -92,6 +92,9 @@ def _load() -> ctypes.CDLL:
     lib.ep_combine.restype = i32
     lib.ep_get_dispatch_layout_noalloc.argtypes = [p, i64, i32, i32, p, p, p, p, p]
     lib.ep_get_dispatch_layout_noalloc.restype = i32
+    lib.ep_sm_partition.argtypes = [i32, ctypes.POINTER(p), ctypes.POINTER(p),
+                                    ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.ep_sm_partition.restype = i32
     lib.ep_selftest_wait_timeout.argtypes = [p, ctypes.c_uint64, p]
     lib.ep_selftest_wait_timeout.restype = i32
     lib.ep_get_status.argtypes = [p, p]
@@ -256,6 +259,17 @@ def ep_combine(expert_out: torch.Tensor, slot: torch.Tensor, topk_w: torch.Tenso
         _ptr(slot, torch.int32, "slot"), _ptr(topk_w, torch.float32, "topk_w"), T, H, K,
         _ptr(y, torch.bfloat16, "y"), _ptr(status, torch.int32, "status"), _stream(stream))
     _check(code, "ep_combine")
+
+
+def ep_sm_partition(num_sms: int) -> Tuple[int, Optional[int], int, int]:
+    """(stream, rest_stream, sms, rest_sms) of an SM partition of at least
+    num_sms SMs on the current device; the streams are raw cudaStream_t
+    handles (wrap them with torch.cuda.ExternalStream)."""
+    s, r = ctypes.c_void_p(), ctypes.c_void_p()
+    n, rn = ctypes.c_int(), ctypes.c_int()
+    _check(lib.ep_sm_partition(int(num_sms), ctypes.byref(s), ctypes.byref(r), ctypes.byref(n),
+                               ctypes.byref(rn)), "ep_sm_partition")
+    return int(s.value), (int(r.value) if r.value else None), n.value, rn.value
 
 
 def ep_selftest_wait_timeout(status: torch.Tensor, limit_ns: int, stream=None) -> None:

@@ -104,9 +104,12 @@ EP_API int ep_get_num_sms(void);
 /* Whether a kernel launch may overlap the tail of the previous kernel on the
  * stream (programmatic dependent launch; each kernel still waits for its
  * predecessor's results before touching global memory):
- *   0  auto (default): only while the SM budget covers the whole GPU. A
- *      smaller budget usually means the GPU is shared with concurrent work,
- *      and there the early launches slowed dispatch + combine measurably.
+ *   0  auto (default): while the SM budget covers the whole GPU, and for
+ *      launches into an SM-partition stream (ep_sm_partition). A smaller
+ *      budget on an ordinary stream usually means the GPU is shared with
+ *      concurrent work, and there an early-launched kernel can land on an SM
+ *      that work keeps busy (measured: the decode step on 24 SMs twice as
+ *      long beside an ALU-bound kernel).
  *   1  always;  2  never.
  * Process-wide, like the SM budget. Returns the stored mode, or -1 (and
  * changes nothing) for any other value. */
@@ -230,6 +233,30 @@ EP_API ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv,
 EP_API ep_status_t ep_get_dispatch_layout_noalloc(const int64_t* topk_idx, int64_t T, int K, int E,
                                                   int32_t* counts, int32_t* offsets, int32_t* slot,
                                                   int32_t* status, void* stream);
+
+/* SM partition: a stream whose kernels the hardware runs on a fixed set of
+ * at least num_sms SMs, and a stream for the device's other SMs (CUDA green
+ * contexts). The pages' SM budget ([DeepEP-TMA] "Minimal SM Occupancy
+ * Configuration": a few SMs for communication, the rest for computation)
+ * limits how many CTAs a kernel launches, not which SMs run them; a
+ * partition fixes those SMs too.
+ *   num_sms     SMs wanted (>= 1); rounded up to the device's partition
+ *               granularity (8 SMs on GB300)
+ *   stream      out: cudaStream_t (as void*) of the partition
+ *   rest_stream out, nullable: cudaStream_t of the remaining SMs (NULL if
+ *               none remain), for the work that runs beside the movement
+ *   sms, rest_sms  out, nullable: SMs of each
+ * On the current device. Calls with the same num_sms on the same device
+ * return the same streams; partitions live until the process exits (the
+ * caller must not destroy the streams). Every call of this library into the
+ * partition stream uses at most its SMs (the budget still applies below
+ * that), and under the default launch-overlap policy (mode 0) may overlap
+ * the previous kernel's tail, since nothing foreign can share those SMs.
+ * Returns EP_ERR_UNSUPPORTED where the driver offers no green contexts or
+ * num_sms exceeds the SM count; EP_ERR_INVALID for num_sms < 1 or a null
+ * `stream`. The pages have no counterpart for the partition itself. */
+EP_API ep_status_t ep_sm_partition(int num_sms, void** stream, void** rest_stream, int* sms,
+                                   int* rest_sms);
 
 /* Self-test of the failure path: launches one warp that waits, for at most
  * `limit_ns` nanoseconds (1 .. 2e9), on an mbarrier nothing completes, so the

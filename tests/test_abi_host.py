@@ -210,6 +210,15 @@ def _raw(ep):
     return ep.lib
 
 
+def test_sm_partition_argument_checks(ep):
+    """Refused before any CUDA call: fewer than one SM, or no stream out."""
+    lib = _raw(ep)
+    s = ctypes.c_void_p()
+    assert lib.ep_sm_partition(0, ctypes.byref(s), None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_sm_partition(-3, ctypes.byref(s), None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_sm_partition(24, None, None, None, None) == ep.EP_ERR_INVALID
+
+
 def test_host_argument_checks(ep):
     lib = _raw(ep)
     A = 0x10000  # a fake, 16-byte aligned "device" address; never dereferenced

@@ -1,5 +1,6 @@
 """Dispatch and combine on a partial SM budget while an arithmetic kernel
-holds the other SMs must give exactly the oracle's results.
+holds the other SMs must give exactly the oracle's results, on ordinary
+streams and in an SM partition.
 
 "How DeepEP Utilizes TMA Instructions for Minimal SM Usage on Hopper GPUs"
 (Minimal SM Occupancy Configuration) limits the communication kernels to a
@@ -119,9 +120,26 @@ def _alu_iters(alu, out, grid, stream, target_ms: float) -> int:
     return max(probe, int(probe * target_ms / max(e0.elapsed_time(e1), 1e-3)))
 
 
+def test_sm_partition_splits_the_device(ep):
+    """ep_sm_partition: at least the SMs asked for, the rest in the second
+    stream, the same streams for the same request."""
+    dev = torch.device("cuda:0")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    s, r, n, rn = ep.ep_sm_partition(BUDGET)
+    assert s and r and n >= BUDGET and n + rn == sms
+    assert ep.ep_sm_partition(BUDGET) == (s, r, n, rn)
+    with pytest.raises(ep.EPError):
+        ep.ep_sm_partition(sms + 1)
+
+
+@pytest.mark.parametrize("where", ["streams", "partition"])
 @pytest.mark.parametrize("mode", [0, 1], ids=["default-policy", "launch-overlap-forced"])
 @pytest.mark.parametrize("shape", ["decode", "T512-H2048"])
-def test_movement_beside_alu_kernel_is_bit_exact(ep, alu, mode, shape):
+def test_movement_beside_alu_kernel_is_bit_exact(ep, alu, mode, shape, where):
+    """`streams`: two ordinary streams, the movement's at high priority.
+    `partition`: the movement in an SM partition of 24 SMs and the ALU
+    kernel in the partition of the other SMs (ep_sm_partition), where the
+    default policy lets the movement's launches overlap."""
     dev = torch.device("cuda:0")
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     if shape == "decode":
@@ -134,10 +152,16 @@ def test_movement_beside_alu_kernel_is_bit_exact(ep, alu, mode, shape):
         wls = [W.Workload(f"ovl-t512-{i}", T=512, H=2048, E=64, K=8, seed=50 + i)
                for i in range(BATCHES)]
     batches = [Batch(ep, wl, dev) for wl in wls]
-    s_move = torch.cuda.Stream(dev, priority=-1)
-    s_alu = torch.cuda.Stream(dev)
+    if where == "partition":
+        h_move, h_alu, n_move, n_alu = ep.ep_sm_partition(BUDGET)
+        s_move = torch.cuda.ExternalStream(h_move, device=dev)
+        s_alu = torch.cuda.ExternalStream(h_alu, device=dev)
+        grid = n_alu
+    else:
+        s_move = torch.cuda.Stream(dev, priority=-1)
+        s_alu = torch.cuda.Stream(dev)
+        grid = sms - BUDGET
     out = torch.zeros(1, device=dev)
-    grid = sms - BUDGET
     try:
         ep.ep_set_num_sms(BUDGET)
         ep.ep_set_launch_overlap(mode)
