@@ -132,6 +132,25 @@ def test_sm_partition_splits_the_device(ep):
         ep.ep_sm_partition(sms + 1)
 
 
+def test_partition_bounds_the_grid_whatever_the_budget(ep):
+    """With the budget at all SMs (0), calls into a 24-SM partition still
+    launch at most the partition's CTAs per copy kernel and give the
+    oracle's results (a larger grid would run in waves, or not at all)."""
+    dev = torch.device("cuda:0")
+    h, _, n, _ = ep.ep_sm_partition(BUDGET)
+    s = torch.cuda.ExternalStream(h, device=dev)
+    wl = W.Workload("partition-budget-0", T=1000, H=2048, E=64, K=6, seed=61)
+    b = Batch(ep, wl, dev)
+    try:
+        ep.ep_set_num_sms(0)
+        b.layout(ep, s)
+        b.move(ep, s)
+        torch.cuda.synchronize()
+        b.check(ep)
+    finally:
+        ep.ep_set_num_sms(0)
+
+
 @pytest.mark.parametrize("where", ["streams", "partition"])
 @pytest.mark.parametrize("mode", [0, 1], ids=["default-policy", "launch-overlap-forced"])
 @pytest.mark.parametrize("shape", ["decode", "T512-H2048"])
