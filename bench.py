@@ -1,10 +1,12 @@
 """Benchmark of the MoE dispatch/combine hot path on GB300.
 
-One step = layout (ep_get_dispatch_layout) + dispatch (ep_dispatch) + combine
-(ep_combine) over one batch of the DeepSeek-V3-shaped prefill workload
-(T=4096 tokens, H=7168 bf16, E=256 experts, top-8), inputs resident in HBM.
-The headline runs on all SMs; the same step is also timed with a 24-SM
-budget. Prints ONE JSON line (rank 0).
+One step = layout + dispatch (ep_layout_dispatch) + combine (ep_combine)
+over one batch of the DeepSeek-V3-shaped prefill workload (T=4096 tokens,
+H=7168 bf16, E=256 experts, top-8), inputs resident in HBM. The headline
+runs on all SMs; the same step is also timed as three calls
+(ep_get_dispatch_layout, ep_dispatch, ep_combine) with a per-kernel
+breakdown, with a 24-SM budget and in a 24-SM partition. Prints ONE JSON
+line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -305,10 +307,12 @@ def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch
 
 
 def time_fused_steps(step: Step, steps: int, warmup: int, dist_on: bool,
-                     stream: torch.cuda.Stream) -> dict:
-    """The same step with layout and dispatch in one call (ep_layout_dispatch);
-    total without events between the kernels, then a pass with them for the
-    per-kernel breakdown (as in time_steps)."""
+                     stream: torch.cuda.Stream, sampler_index: int = -1) -> dict:
+    """The step with layout and dispatch in one call (ep_layout_dispatch), the
+    headline: W untimed steps, then exactly K steps between barrier +
+    synchronize, CUDA events on the launching stream around the loop only
+    (the SM clock sampled meanwhile); then a pass with events between the
+    calls for the per-call breakdown (as in time_steps)."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             step.run_fused(step.b, stream)
@@ -316,11 +320,16 @@ def time_fused_steps(step: Step, steps: int, warmup: int, dist_on: bool,
         end = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         barrier(dist_on)
+        sampler = ClockSampler(sampler_index) if sampler_index >= 0 else None
+        if sampler:
+            sampler.__enter__()
         start.record(stream)
         for _ in range(steps):
             step.run_fused(step.b, stream)
         end.record(stream)
         torch.cuda.synchronize()
+        if sampler:
+            sampler.__exit__(None, None, None)
         barrier(dist_on)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
         for i in range(steps):
@@ -333,11 +342,13 @@ def time_fused_steps(step: Step, steps: int, warmup: int, dist_on: bool,
         torch.cuda.synchronize()
     return {"total_ms": start.elapsed_time(end),
             "layout_dispatch_ms": [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)],
-            "combine_ms": [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]}
+            "combine_ms": [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)],
+            "clocks": sampler.summary() if sampler else None}
 
 
 def time_e2e(step: Step, inp: W.Inputs, steps: int, warmup: int) -> dict:
-    """The same step through the public API with host-resident inputs: every
+    """The headline step (ep_layout_dispatch + ep_combine) through the public
+    API with host-resident inputs: every
     step copies x, topk_idx and topk_w from pinned host memory to the device
     and reads y back, inside the timed region. Two device buffer sets and
     separate copy streams let step i's copies overlap step i-1's kernels,
@@ -369,7 +380,7 @@ def time_e2e(step: Step, inp: W.Inputs, steps: int, warmup: int) -> dict:
         with torch.cuda.stream(s_run):
             s_run.wait_event(ready)
             s_run.wait_event(out[j])
-            step.run(b, s_run)
+            step.run_fused(b, s_run)
             done[j].record(s_run)
         with torch.cuda.stream(s_out):
             s_out.wait_event(done[j])
@@ -683,14 +694,16 @@ def budget_ceiling_frac(c: dict | None, s: dict, step) -> dict | None:
 def time_workload(ep, dev, wl: W.Workload, budget: int, steps: int, warmup: int,
                   peak: float) -> dict:
     """One workload at one SM budget: K steps back to back (events only
-    around the loop), the same step captured once in a CUDA graph and
-    replayed K times, and a pass with events between the kernels for the
-    per-kernel medians. Inputs resident in HBM."""
+    around the loop) as three calls and with ep_layout_dispatch, the
+    three-call step captured once in a CUDA graph and replayed K times, and
+    a pass with events between the kernels for the per-kernel medians.
+    Inputs resident in HBM."""
     step = Step(ep, W.make_inputs(wl), dev)
     sms_all = torch.cuda.get_device_properties(dev).multi_processor_count
     ep.ep_set_num_sms(budget)
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
+        frun = time_fused_steps(step, steps, warmup, False, stream)
         run = time_steps(step, steps, warmup, False, stream)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -719,6 +732,9 @@ def time_workload(ep, dev, wl: W.Workload, budget: int, steps: int, warmup: int,
         "workload": wl_desc(wl), "num_sms": min(budget or sms_all, sms_all),
         "steps": steps,
         "ms_per_step": round(ms, 5), "tokens_per_s": round(wl.T / (ms * 1e-3)),
+        # layout + dispatch through ep_layout_dispatch, then ep_combine
+        "fused_ms_per_step": round(frun["total_ms"] / steps, 5),
+        "fused_tokens_per_s": round(wl.T / (frun["total_ms"] / steps * 1e-3)),
         "graph_ms_per_step": round(gms, 5), "graph_tokens_per_s": round(wl.T / (gms * 1e-3)),
         "step_gbs": round((moved + ab["layout"]) / (min(ms, gms) * 1e-3) / 1e9, 1),
         "kernel_us_median": {k: round(v, 2) for k, v in med.items()},
@@ -1329,13 +1345,18 @@ def main():
     sms_all = torch.cuda.get_device_properties(dev).multi_processor_count
 
     ep.ep_set_num_sms(0)
-    main_run = time_steps(step, args.steps, args.warmup, dist_on, stream, sampler_index=local)
     if args.only_main:
+        main_run = time_steps(step, args.steps, args.warmup, dist_on, stream)
         ms = max_over_ranks(main_run["total_ms"] / args.steps, dist_on)
         if rank == 0:
             print(json.dumps({"only_main": True, "ms_per_step": ms,
                               "tokens_per_s": world * step.T / (ms * 1e-3)}), flush=True)
         return
+    # the headline: layout + dispatch through ep_layout_dispatch, then combine
+    fused_run = time_fused_steps(step, args.steps, args.warmup, dist_on, stream,
+                                 sampler_index=local)
+    # the same step as three calls, with its per-kernel breakdown
+    main_run = time_steps(step, args.steps, args.warmup, dist_on, stream)
     ep.ep_set_num_sms(args.budget_sms)
     budget_run = time_steps(step, args.steps, args.warmup, dist_on, stream)
     # the same budget as an SM partition (ep_sm_partition): its kernels stay
@@ -1348,8 +1369,6 @@ def main():
                                   torch.cuda.ExternalStream(h, device=dev))
         except Exception as e:  # noqa: BLE001 - reported in the line
             log(f"SM partition unavailable: {e}")
-    ep.ep_set_num_sms(0)
-    fused_run = time_fused_steps(step, args.steps, args.warmup, dist_on, stream)
     ep.ep_set_num_sms(args.budget_sms)
     fused_budget = time_fused_steps(step, args.steps, args.warmup, dist_on, stream)
     ep.ep_set_num_sms(0)
@@ -1410,16 +1429,20 @@ def main():
     traffic = kernel_traffic(dom)
     e2e_ms = max_over_ranks(e2e["ms_per_step"], dist_on)
 
+    # every summary takes a max over ranks: computed on all ranks, in order
+    head = summarize_fused(fused_run, sms_all)
+    fused_bud = summarize_fused(fused_budget, min(args.budget_sms, sms_all))
+    part_sum = summarize(part_run, part_sms) if part_run else None
     if rank == 0:
         cpu = None if args.no_cpu_baseline else cpu_baseline(inp)
         line = {
             "metric": METRIC,
-            "value": s_all["tokens_per_s"],
+            "value": head["tokens_per_s"],
             "unit": "tokens/s",
             "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup,
-            "ms_per_step": s_all["ms_per_step"],
+            "ms_per_step": head["ms_per_step"],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
@@ -1427,6 +1450,9 @@ def main():
             "data": "synthetic",
             "config": {
                 "workload": wl_desc(wl),
+                "step": "ep_layout_dispatch (layout + dispatch) then ep_combine; the same "
+                        "step as three calls (ep_get_dispatch_layout, ep_dispatch, "
+                        "ep_combine) is hbm.all_sms",
                 "num_sms": sms_all,
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                 "accumulate": "fp32 (combine)",
@@ -1436,11 +1462,9 @@ def main():
             "hbm": {
                 "all_sms": s_all,
                 f"sms_{args.budget_sms}": s_bud,
-                "fused_all_sms": summarize_fused(fused_run, sms_all),
-                f"fused_sms_{args.budget_sms}": summarize_fused(fused_budget,
-                                                                min(args.budget_sms, sms_all)),
-                f"partition_sms_{args.budget_sms}": (summarize(part_run, part_sms)
-                                                     if part_run else None),
+                "fused_all_sms": head,
+                f"fused_sms_{args.budget_sms}": fused_bud,
+                f"partition_sms_{args.budget_sms}": part_sum,
                 "peak_gbs": peak,
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_step": ab,
@@ -1482,7 +1506,7 @@ def main():
                                  / (e2e_ms * 1e-3) / 1e9,
             },
             "gpu_launches": step.launches_per_step * args.steps,
-            "clocks": main_run["clocks"],
+            "clocks": fused_run["clocks"],
             "cpu_baseline": cpu,
             "decode_latency": decode,
         }

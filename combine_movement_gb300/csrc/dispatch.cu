@@ -226,8 +226,6 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
         fence_mbar_init();
     }
     __syncwarp();
-    griddep_wait();
-    griddep_launch_dependents();
 
     const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
@@ -269,6 +267,18 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
                   a.x + t * static_cast<int64_t>(a.row_bytes) + off, bytes, bar, pol_load);
     };
 
+    auto first_loads = [&]() {
+        for (int64_t j = 0; j < P && j < n; ++j) issue_load(j);
+    };
+    // Every global-memory access waits for the previous kernel on the stream
+    // (programmatic dependent launch), except the first row loads when x is
+    // known to be complete already (a.x_ready: the layout kernel of
+    // ep_layout_dispatch precedes this launch); they then overlap it.
+    const bool early = !FUSED && a.x_ready != 0;
+    if (early) first_loads();
+    griddep_wait();
+    griddep_launch_dependents();
+
     // The fused kernel's entries: the CTA's slots stay in shared memory
     // (own_slot) when f.own_off != 0.
     const CtaEntries own = FUSED ? cta_entries(a, units, nw_total) : CtaEntries{0, 0};
@@ -293,12 +303,9 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     // before the fused kernel computes it, right behind its routing-table
     // loads (every thread of the CTA then takes part in the layout, whatever
     // its own share of units).
-    auto first_loads = [&]() {
-        for (int64_t j = 0; j < P && j < n; ++j) issue_load(j);
-    };
     if (FUSED)
         fused_layout(a, f, smem, own, first_loads);
-    else
+    else if (!early)
         first_loads();
     if (n <= 0) return;
 

@@ -114,6 +114,11 @@ bool use_combine_tma(int K, int num_sms) {
     return false;
 }
 
+// Routing tables of at most this many entries are laid out by every CTA of
+// the one-launch ep_layout_dispatch (a whole-table pass per CTA); larger ones
+// take the layout kernel and dispatch as two launches.
+constexpr int64_t kFusedMaxEntries = 4096;
+
 // Host checks shared by ep_dispatch and ep_layout_dispatch.
 ep_status_t check_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const int32_t* slot,
                            const float* topk_w, int64_t num_recv, const uint16_t* recv_x,
@@ -293,6 +298,27 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
     if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int n = sms_for_stream(sm_count, s);
+    // Two launches (the layout kernel, then dispatch) when the layout needs
+    // no workspace and either the table is too large for every CTA to
+    // histogram it cheaply, or launches may overlap on this stream (then the
+    // second launch costs nothing). Dispatch's first row loads then overlap
+    // the layout: its predecessor is that layout kernel, which does not
+    // write x. Otherwise one launch does both.
+    if (T > 0) {
+        const ep::LayoutPlan lp = ep::plan_layout(T * K, E);
+        if (lp.workspace_bytes == 0 &&
+            (T * K > kFusedMaxEntries || ep::launch_overlap_allowed(s))) {
+            cudaError_t e = ep::launch_layout(topk_idx, T * K, E, counts, offsets, slot, nullptr,
+                                              lp, status, s);
+            if (e != cudaSuccess) return EP_ERR_CUDA;
+            ep::DispatchArgs a{};
+            st = plan_dispatch(&a, x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src,
+                               status, smem_optin, 0, n, false, s);
+            if (st != EP_OK) return st;
+            a.x_ready = 1;
+            return from_cuda(ep::launch_dispatch(a, n, smem_optin, s));
+        }
+    }
     ep::DispatchArgs a{};
     // histograms, 16-byte alignment, the CTA's own keys and slots
     const size_t hist = 2 * sizeof(int32_t) * static_cast<size_t>(E) + 16 + ep::kFusedOwnBytes;

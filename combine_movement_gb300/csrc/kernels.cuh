@@ -80,6 +80,11 @@ struct DispatchArgs {
     uint32_t n_chunks;     // chunks per row
     uint32_t stage_bytes;  // shared-memory bytes per ring stage (>= chunk_bytes)
     int ring_stages;       // ring stages the rows were planned for (host side)
+    // 1: x was complete before this kernel's predecessor on the stream began
+    // (that predecessor is this library's layout kernel, launched just
+    // before by ep_layout_dispatch, which never writes x), so the first row
+    // loads may go out before the kernel waits for its predecessor.
+    int x_ready;
 };
 
 // Routing inputs and layout outputs of the fused layout + dispatch kernel.

@@ -180,14 +180,20 @@ EP_API ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K,
                         uint16_t* recv_x, float* recv_w, int32_t* recv_src,
                         int32_t* status, void* stream);
 
-/* Layout and dispatch in one launch: the results of ep_get_dispatch_layout
+/* Layout and dispatch in one call: the results of ep_get_dispatch_layout
  * (counts, offsets, slot) and of ep_dispatch (recv_x, recv_w, recv_src),
- * identical to calling the two in turn, with no workspace. Every CTA reads
- * the whole routing table and histograms it in shared memory to lay out its
- * own tokens, so its cost grows with T*K per CTA: it suits decode-size
- * batches only (on GB300, T=128 top-8, a layout + dispatch + combine step
- * with it takes 17 us, with the two separate calls 16 us, their launches
- * overlapping; prefill-size tables are much faster with the separate calls).
+ * identical to calling the two in turn, with no workspace argument.
+ *  - Small tables (at most 4096 entries) on a stream where launches may not
+ *    overlap (a partial SM budget on an ordinary stream): one launch in
+ *    which every CTA reads the whole routing table and lays out its own
+ *    tokens (on GB300, T=128 top-8 on 24 SMs: a layout + dispatch + combine
+ *    step takes 29.4 us with it, 33.4 us with the separate calls).
+ *  - Otherwise, when the layout needs no workspace (at most 65,536 entries
+ *    at E <= 256): the layout kernel and the dispatch kernel, with
+ *    dispatch's first row loads issued while the layout runs (safe because
+ *    this call launched that layout kernel itself, which never writes x).
+ *  - Larger tables fall back to the one-launch form, whose cost grows with
+ *    T*K per CTA; call the two functions separately for those.
  * Arguments as in those two calls; T == 0 still writes zero counts and
  * offsets. */
 EP_API ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64_t T,
