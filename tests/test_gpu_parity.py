@@ -452,7 +452,7 @@ def test_cuda_graph_capture_and_replay(ep, T, H, E, K):
         ep.ep_set_num_sms(0)
 
 
-# ---- ep_layout_dispatch: layout and dispatch in one launch -----------------
+# ---- ep_layout_dispatch: layout and dispatch in one call (one or two launches)
 
 @pytest.mark.parametrize("name,budgets", [
     ("tiny", (0, 3)),
