@@ -44,6 +44,8 @@ using SmResourceSplitByCountFn = CUresult (*)(CUdevResource*, unsigned int*, con
 using DevResourceGenerateDescFn = CUresult (*)(CUdevResourceDesc*, CUdevResource*, unsigned int);
 using GreenCtxCreateFn = CUresult (*)(CUgreenCtx*, CUdevResourceDesc, CUdevice, unsigned int);
 using GreenCtxStreamCreateFn = CUresult (*)(CUstream*, CUgreenCtx, unsigned int, int);
+using GreenCtxDestroyFn = CUresult (*)(CUgreenCtx);
+using StreamDestroyFn = CUresult (*)(CUstream);
 
 struct DriverApi {
     DeviceGetFn device_get = nullptr;
@@ -52,6 +54,8 @@ struct DriverApi {
     DevResourceGenerateDescFn gen_desc = nullptr;
     GreenCtxCreateFn green_create = nullptr;
     GreenCtxStreamCreateFn green_stream = nullptr;
+    GreenCtxDestroyFn green_destroy = nullptr;
+    StreamDestroyFn stream_destroy = nullptr;
     bool ok = false;
 };
 
@@ -77,7 +81,9 @@ const DriverApi& driver() {
                entry_point("cuDevSmResourceSplitByCount", &a.split) &&
                entry_point("cuDevResourceGenerateDesc", &a.gen_desc) &&
                entry_point("cuGreenCtxCreate", &a.green_create) &&
-               entry_point("cuGreenCtxStreamCreate", &a.green_stream);
+               entry_point("cuGreenCtxStreamCreate", &a.green_stream) &&
+               entry_point("cuGreenCtxDestroy", &a.green_destroy) &&
+               entry_point("cuStreamDestroy", &a.stream_destroy);
         return a;
     }();
     return api;
@@ -96,13 +102,18 @@ std::mutex g_mu;
 std::vector<Partition> g_parts;
 
 // A green context on `res` and a non-blocking stream in it.
-ep_status_t make_stream(const DriverApi& d, CUdevice dev, CUdevResource* res, cudaStream_t* out) {
+ep_status_t make_stream(const DriverApi& d, CUdevice dev, CUdevResource* res, CUgreenCtx* ctx,
+                        cudaStream_t* out) {
     CUdevResourceDesc desc = nullptr;
     if (d.gen_desc(&desc, res, 1) != CUDA_SUCCESS) return EP_ERR_CUDA;
     CUgreenCtx g = nullptr;
     if (d.green_create(&g, desc, dev, CU_GREEN_CTX_DEFAULT_STREAM) != CUDA_SUCCESS) return EP_ERR_CUDA;
     CUstream s = nullptr;
-    if (d.green_stream(&s, g, CU_STREAM_NON_BLOCKING, 0) != CUDA_SUCCESS) return EP_ERR_CUDA;
+    if (d.green_stream(&s, g, CU_STREAM_NON_BLOCKING, 0) != CUDA_SUCCESS) {
+        d.green_destroy(g);
+        return EP_ERR_CUDA;
+    }
+    *ctx = g;
     *out = reinterpret_cast<cudaStream_t>(s);
     return EP_OK;
 }
@@ -159,11 +170,16 @@ extern "C" ep_status_t ep_sm_partition(int num_sms, void** stream, void** rest_s
     p.requested = num_sms;
     p.sms = static_cast<int>(group.sm.smCount);
     p.rest_sms = static_cast<int>(remaining.sm.smCount);
-    ep_status_t st = make_stream(d, cu_dev, &group, &p.stream);
+    CUgreenCtx g_part = nullptr, g_rest = nullptr;
+    ep_status_t st = make_stream(d, cu_dev, &group, &g_part, &p.stream);
     if (st != EP_OK) return st;
     if (p.rest_sms > 0) {
-        st = make_stream(d, cu_dev, &remaining, &p.rest);
-        if (st != EP_OK) return st;
+        st = make_stream(d, cu_dev, &remaining, &g_rest, &p.rest);
+        if (st != EP_OK) {  // leave nothing half-made behind
+            d.stream_destroy(reinterpret_cast<CUstream>(p.stream));
+            d.green_destroy(g_part);
+            return st;
+        }
     }
     g_parts.push_back(p);
     *stream = p.stream;
