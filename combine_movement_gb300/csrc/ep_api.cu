@@ -71,15 +71,23 @@ int sms_for_stream(int sm_count, cudaStream_t stream) {
 }  // namespace
 
 namespace ep {
+
+namespace {
+thread_local int64_t t_call_bytes = 0;
+}  // namespace
+
+CallBytes::CallBytes(int64_t bytes) : saved_(t_call_bytes) { t_call_bytes = bytes; }
+CallBytes::~CallBytes() { t_call_bytes = saved_; }
+
 // Programmatic dependent launch (see launch_dependent): in the default mode
-// while the SM budget covers the whole current device, or for a launch into
-// an SM-partition stream.
+// while the SM budget covers the whole current device, or for a launch of a
+// decode-size call into an SM-partition stream.
 bool launch_overlap_allowed(cudaStream_t stream) {
     if (!EP_PDL) return false;
     const int mode = g_overlap_mode.load(std::memory_order_relaxed);
     if (mode == 1) return true;
     if (mode == 2) return false;
-    if (partition_sms(stream) > 0) return true;
+    if (partition_sms(stream) > 0) return t_call_bytes <= kPartitionOverlapBytes;
     int c = 0, s = 0;
     if (!device_limits(&c, &s)) return false;
     return sms_in_effect(c) == c;
@@ -270,6 +278,7 @@ ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const in
     ep_status_t st = check_dispatch(x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src,
                                     status);
     if (st != EP_OK || T == 0) return st;
+    const ep::CallBytes call_bytes(T * K * 2 * H);
     int sm_count = 0, smem_optin = 0;
     if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -294,6 +303,7 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
     ep_status_t st = check_dispatch(x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src,
                                     status);
     if (st != EP_OK) return st;
+    const ep::CallBytes call_bytes(T * K * 2 * H);
     int sm_count = 0, smem_optin = 0;
     if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -348,6 +358,7 @@ ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv, const int32
     if (!aligned(expert_out, 16) || !aligned(y, 16) || !aligned(slot, 4) || !aligned(topk_w, 4) ||
         !aligned(status, 4))
         return EP_ERR_INVALID;
+    const ep::CallBytes call_bytes(T * K * 2 * H);
     int sm_count = 0, smem_optin = 0;
     if (!device_limits(&sm_count, &smem_optin)) return EP_ERR_CUDA;
     ep::CombineArgs a{};

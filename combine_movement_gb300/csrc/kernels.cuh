@@ -149,17 +149,17 @@ cudaError_t launch_combine_tma(const CombineArgs& a, int num_sms, int smem_optin
 // launch may start while the previous kernel on the stream finishes: its CTAs
 // become resident and wait in griddep_wait(), which every such kernel calls
 // before touching global memory, so the launch latency overlaps the previous
-// kernel's tail. On the DeepSeek-V3 prefill step this saves ~2 us of ~193;
-// on the decode step (T=128) 3-5 us of ~21-41.
+// kernel's tail. On the DeepSeek-V3 prefill step this saves ~2 us of ~180;
+// on the decode step (T=128) 3-8 us of ~16-39.
 // By default it is used only while the SM budget covers the whole GPU, or
-// for launches into an SM-partition stream (launch_overlap_allowed). A
-// smaller budget on an ordinary stream means the GPU is shared with
-// concurrent work on SMs the hardware picks, and there an early-launched
-// kernel may land on an SM the foreign work keeps busy: beside an ALU-bound
-// kernel on the other SMs, the decode step on 24 SMs took twice as long with
-// early launches, and prefill dispatch + combine 3-6 % longer. A partition
-// stream's kernels run only on the partition's SMs, where nothing foreign
-// can sit.
+// for decode-size calls into an SM-partition stream
+// (launch_overlap_allowed). A smaller budget on an ordinary stream means
+// the GPU is shared with concurrent work on SMs the hardware picks, and
+// there an early-launched kernel may land on an SM the foreign work keeps
+// busy: beside an ALU-bound kernel on the other SMs, the decode step on 24
+// SMs took twice as long with early launches, and prefill dispatch +
+// combine 3-6 % longer. A partition stream's kernels run only on the
+// partition's SMs, where nothing foreign can sit.
 #ifndef EP_PDL
 #define EP_PDL 1
 #endif
@@ -168,6 +168,25 @@ bool launch_overlap_allowed(cudaStream_t stream);
 // SMs of the partition `stream` belongs to (ep_sm_partition), or 0 for any
 // other stream.
 int partition_sms(cudaStream_t stream);
+
+// Row bytes the current C ABI call moves (0 for the layout), set for the
+// call's duration by its entry point. Inside an SM partition, launches
+// overlap only for calls that move at most kPartitionOverlapBytes
+// (decode-size batches): there the early launches take the decode step on
+// 24 SMs from ~30 to ~22 us, while a prefill-size call measured 3-5 %
+// slower with them than without (the next kernel's CTAs then wait for the
+// partition's own SMs to drain).
+constexpr int64_t kPartitionOverlapBytes = int64_t{64} << 20;
+class CallBytes {
+  public:
+    explicit CallBytes(int64_t bytes);
+    ~CallBytes();
+    CallBytes(const CallBytes&) = delete;
+    CallBytes& operator=(const CallBytes&) = delete;
+
+  private:
+    int64_t saved_;
+};
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent(void (*kernel)(KArgs...), int grid, int block, size_t smem,
