@@ -19,6 +19,7 @@ same workload, timed as the reference arm.
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import os
@@ -579,7 +580,12 @@ def decode_latency(ep, dev, budgets=(16, 24, 0), ceilings: dict | None = None) -
     launch overlap forced on. Each kernel's figure is also given net of the
     event-to-event time of an empty launch, and against what its n SMs can
     move (write ceiling for dispatch, read ceiling for combine; L2-resident
-    probes, since the warm step's data sits in L2)."""
+    probes, since the warm step's data sits in L2). Short launches are also
+    timed back to back, beside plain 16-byte write-only and read-only
+    kernels over the same receive-row bytes on the same n SMs: per launch,
+    at this size, ramp and launch spacing weigh as much as bandwidth, and
+    those probes are the floor a kernel moving these bytes meets."""
+    import ctypes
     wl = W.DECODE
     step = Step(ep, W.make_inputs(wl), dev)
     flush = _Flusher(dev)
@@ -589,6 +595,14 @@ def decode_latency(ep, dev, budgets=(16, 24, 0), ceilings: dict | None = None) -
     overhead = empty_launch_us()
     out = {"workload": wl_desc(wl), "empty_launch_us": round(overhead, 2)}
     mode0 = ep.ep_get_launch_overlap()
+    try:
+        L = _probe_lib()
+    except Exception as e:  # noqa: BLE001 - reported, not fatal
+        log(f"same-size probes unavailable: {e}")
+        L = None
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    probe_buf = torch.empty(rows, dtype=torch.uint8, device=dev)
     for b in budgets:
         n = min(b or sms_all, sms_all)
         ep.ep_set_num_sms(b)
@@ -623,6 +637,22 @@ def decode_latency(ep, dev, budgets=(16, 24, 0), ceilings: dict | None = None) -
             return e0.elapsed_time(e1) / n_ * 1e3
         out_b2b = back_to_back(lambda: step.run(step.b))
         graph_b2b = back_to_back(g.replay)
+        k_b2b = {"layout": back_to_back(lambda: step.layout(step.b)),
+                 "dispatch": back_to_back(lambda: step.dispatch(step.b)),
+                 "combine": back_to_back(lambda: step.combine(step.b))}
+        probes = None
+        if L is not None:
+            # one 1024-thread CTA per SM over the receive-row bytes; the read
+            # goes over rows the write just left in L2, as combine's do
+            def p_write():
+                if L.bw_write(vp(probe_buf.data_ptr()), sz(rows), n, 1024) != 0:
+                    raise RuntimeError("probe launch failed")
+
+            def p_read():
+                if L.bw_read(vp(probe_buf.data_ptr()), sz(rows), vp(sink.data_ptr()), n, 1024) != 0:
+                    raise RuntimeError("probe launch failed")
+            probes = {"write": back_to_back(p_write), "read": back_to_back(p_read),
+                      "empty": back_to_back(lambda: torch.cuda._sleep(0))}
         net = {k: max(v - overhead, 1e-3) for k, v in
                (("layout", k_lay), ("dispatch", k_dis), ("combine", k_com))}
         entry = {
@@ -640,7 +670,19 @@ def decode_latency(ep, dev, budgets=(16, 24, 0), ceilings: dict | None = None) -
             "kernel_us": {"layout": round(k_lay, 2), "dispatch": round(k_dis, 2),
                           "combine": round(k_com, 2)},
             "kernel_net_us": {k: round(v, 2) for k, v in net.items()},
+            # each kernel launched 500 times back to back, per launch
+            "kernel_back_to_back_us": {k: round(v, 2) for k, v in k_b2b.items()},
         }
+        if probes:
+            entry["same_size_probes_back_to_back_us"] = {
+                k: round(v, 2) for k, v in probes.items()}
+            entry["same_size_probes_source"] = (
+                f"16-byte streaming write-only / read-only kernels over the {rows} receive-row "
+                f"bytes on {n} SMs (one 1024-thread CTA per SM), read after write (L2-resident)")
+            # probe time / kernel time, both back to back: 1.0 = as fast as a
+            # plain stream of the same bytes on the same SMs
+            entry["dispatch_frac_of_same_size_write"] = round(probes["write"] / k_b2b["dispatch"], 3)
+            entry["combine_frac_of_same_size_read"] = round(probes["read"] / k_b2b["combine"], 3)
         if 0 < b < sms_all:
             # the same step in an SM partition of b SMs (ep_sm_partition): the
             # hardware keeps its kernels on those SMs, and the default policy
@@ -670,6 +712,7 @@ def decode_latency(ep, dev, budgets=(16, 24, 0), ceilings: dict | None = None) -
         out[f"sms_{b or 'all'}"] = entry
         del g
     ep.ep_set_num_sms(0)
+    del probe_buf
     return out
 
 
@@ -950,8 +993,10 @@ int ring_store(void* dst, long long units, unsigned chunk, int K, int grid, int 
 """
 
 
+@functools.lru_cache(maxsize=1)
 def _probe_lib():
-    """The probes above, built with nvcc into a temporary directory."""
+    """The probes above, built with nvcc into a temporary directory (once per
+    process)."""
     import ctypes
     import tempfile
     tmp = tempfile.mkdtemp(prefix="ep_probes_")

@@ -20,8 +20,9 @@
 // device's partition granularity, 8 SMs on GB300) and makes one stream for
 // them and one for the SMs that remain. Launches of this library into a
 // partition stream use at most the partition's SMs and, under the default
-// launch-overlap policy, may overlap the previous kernel's tail: nothing
-// foreign can share those SMs. Other work goes into the rest stream.
+// launch-overlap policy, those of decode-size calls may overlap the previous
+// kernel's tail: nothing foreign can share those SMs. Other work goes into
+// the rest stream.
 //
 // The driver functions are reached through the runtime's driver entry
 // points, so the library links no driver library. Partitions are created

@@ -158,7 +158,8 @@ def test_movement_beside_alu_kernel_is_bit_exact(ep, alu, mode, shape, where):
     """`streams`: two ordinary streams, the movement's at high priority.
     `partition`: the movement in an SM partition of 24 SMs and the ALU
     kernel in the partition of the other SMs (ep_sm_partition), where the
-    default policy lets the movement's launches overlap."""
+    default policy lets the launches of these calls overlap (both shapes
+    move at most 64 MB of rows per call)."""
     dev = torch.device("cuda:0")
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     if shape == "decode":
