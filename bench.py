@@ -67,16 +67,24 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
 
 
+def sources_sha256(names) -> str:
+    """sha256 over the named kernel sources (csrc/), concatenated in order."""
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "combine_movement_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch from a committed ncu summary, or None if absent
-    or taken on a different version of the kernel source."""
+    or taken on a different version of the kernel's sources (the .cu and
+    the headers it includes)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)[kernel]
-        src = os.path.join(ROOT, "combine_movement_gb300", "csrc", rec["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if h != rec["source_sha256"]:
+        if sources_sha256(rec["sources"]) != rec["sources_sha256"]:
             return None
         return int(rec["bytes_per_launch"])
     except Exception:
