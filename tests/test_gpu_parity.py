@@ -246,6 +246,8 @@ def test_random_shapes(ep, T, H, E, K, mask, routing, budget, seed):
     num_recv = R_valid + 1
     ref = oracle_path(inp, num_recv, 1.5)
     assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget), ref)
+    # the same case through ep_layout_dispatch (one or two launches)
+    assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget, fused=True), ref)
 
 
 def test_empty_batch(ep):
