@@ -109,19 +109,26 @@ __device__ __forceinline__ void fused_layout(const DispatchArgs& a, const FusedL
         if (keep && i >= i0 && i < i1) own_key[i - i0] = static_cast<int16_t>(e);
     };
     // 16-byte loads (two ids each), 16 in flight per thread; an 8-byte-
-    // aligned first id and an odd last id are read on their own.
+    // aligned first id and an odd last id are read on their own. The trip
+    // count is the same for every lane of a warp (w0 is the warp's first
+    // lane), so prefetch() and its bulk copies always run in a converged
+    // warp, as in the ring: a warp split by a per-lane bound faulted with a
+    // misaligned address on its first bulk loads (150 ids on one CTA).
     const int64_t head = (reinterpret_cast<uintptr_t>(f.idx) & 15u) ? 1 : 0;
     const int64_t pairs = N > head ? (N - head) / 2 : 0;
     const longlong2* pv = reinterpret_cast<const longlong2*>(f.idx + head);
     constexpr int kBatch = 16;
     bool prefetched = false;
-    for (int64_t b0 = threadIdx.x; b0 < pairs; b0 += static_cast<int64_t>(blockDim.x) * kBatch) {
+    for (int64_t w0 = threadIdx.x & ~31u; w0 < pairs;
+         w0 += static_cast<int64_t>(blockDim.x) * kBatch) {
+        const int64_t b0 = w0 + lane;
         longlong2 v[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int64_t q = b0 + static_cast<int64_t>(u) * blockDim.x;
             v[u] = q < pairs ? __ldg(pv + q) : make_longlong2(-1, -1);
         }
+        __syncwarp();
         if (!prefetched) {
             prefetch();
             prefetched = true;
@@ -135,6 +142,7 @@ __device__ __forceinline__ void fused_layout(const DispatchArgs& a, const FusedL
             }
         }
     }
+    __syncwarp();
     if (!prefetched) prefetch();
     if (threadIdx.x == 0) {
         if (head && N > 0) count(0, __ldg(f.idx));

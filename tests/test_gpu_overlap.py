@@ -27,6 +27,7 @@ import torch
 
 import oracle
 from combine_movement_gb300 import workloads as W
+from test_gpu_parity import _custom, assert_parity, gpu_path, oracle_path
 
 pytestmark = pytest.mark.gpu
 
@@ -215,3 +216,32 @@ def test_movement_beside_alu_kernel_is_bit_exact(ep, alu, mode, shape, where):
     finally:
         ep.ep_set_num_sms(0)
         ep.ep_set_launch_overlap(0)
+
+
+@pytest.mark.parametrize("T,H,E,K,mask", [
+    (128, 7168, 256, 8, 0.0),   # decode: 14.7 MB of rows, launches overlap in the partition
+    (555, 7168, 64, 8, 0.0),    # 63.7 MB: just under the 64 MB size rule
+    (600, 7168, 64, 8, 0.0),    # 68.8 MB: just over it, ordinary launch order
+    (1000, 2056, 40, 6, 0.1),   # masked entries, rows not a multiple of the column block
+    (3, 24, 2, 2, 0.0),         # tiny rows
+    (4096, 1024, 128, 8, 0.0),  # 67 MB, a multi-CTA layout
+])
+@pytest.mark.parametrize("fused", [False, True], ids=["three-calls", "layout-dispatch"])
+def test_partition_stream_matches_oracle(ep, T, H, E, K, mask, fused):
+    """Every call of the path into a 24-SM partition stream (the default
+    launch policy: overlapping launches for calls of at most 64 MB of rows,
+    ordinary order above), at the budget of all SMs and of 5, gives the
+    oracle's results."""
+    dev = torch.device("cuda:0")
+    h, _, _, _ = ep.ep_sm_partition(BUDGET)
+    s = torch.cuda.ExternalStream(h, device=dev)
+    inp = _custom(T, H, E, K, seed=T + E, mask=mask)
+    num_recv = int((inp.topk_idx >= 0).sum()) + 2
+    ref = oracle_path(inp, num_recv, 1.5)
+    try:
+        for b in (0, 5):
+            with torch.cuda.stream(s):
+                got = gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=b, stream=s, fused=fused)
+            assert_parity(got, ref)
+    finally:
+        ep.ep_set_num_sms(0)

@@ -487,6 +487,25 @@ def test_fused_layout_dispatch_edges(ep, T, H, E, K, mask):
         assert_parity(gpu_path(ep, inp, R_valid + 3, ref.expert_out, num_sms=b, fused=True), ref)
 
 
+@pytest.mark.parametrize("T,H,E,K,budget", [
+    (150, 3096, 128, 1, 1),   # 75 id pairs: warp 2 split by the id count, rows to move; 205 KB of shared memory
+    (150, 3096, 128, 1, 2),
+    (91, 6200, 64, 2, 1),     # 91 pairs: warp 2 split
+    (77, 5600, 33, 3, 1),     # odd entry count: the last id read on its own
+    (300, 1032, 256, 1, 3),   # 150 pairs: warp 4 split
+    (40, 7168, 16, 5, 1),     # 100 pairs: warp 3 split; two chunks per row
+])
+def test_fused_one_launch_warps_split_by_the_id_count(ep, T, H, E, K, budget):
+    """The one-launch ep_layout_dispatch (small tables on a partial budget)
+    with fewer 16-byte id pairs than threads, not a multiple of 32: one
+    warp's lanes straddle the end of the table while the warp also has
+    rows to move, and the CTA keeps its entries in shared memory."""
+    inp = _custom(T, H, E, K, seed=T + H)
+    num_recv = T * K + 1
+    ref = oracle_path(inp, num_recv, 1.5)
+    assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget, fused=True), ref)
+
+
 def test_fused_layout_dispatch_bad_ids(ep):
     inp = _custom(300, 64, 32, 4)
     idx = inp.topk_idx.clone()
