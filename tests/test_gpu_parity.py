@@ -239,6 +239,35 @@ def _fuzz_cases(n=24, seed=2024):
     return cases
 
 
+def _fuzz_small_cases(n=24, seed=4048):
+    """Seeded random small tables (at most 4096 routing entries) on partial
+    budgets: the shapes that take ep_layout_dispatch's one-launch form, where
+    every CTA lays out the table itself before its ring starts."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        E = int(rng.choice([1, 2, 5, 16, 33, 128, 256, 1000, 4096]))
+        K = int(rng.integers(1, min(E, 8) + 1))
+        T = int(rng.integers(1, 4096 // K + 1))
+        H = 8 * int(rng.integers(1, 1025))
+        while T * H > 3_000_000:
+            T = max(1, T // 2)
+        mask = float(rng.choice([0.0, 0.0, 0.1, 0.5]))
+        routing = "zipf" if (rng.random() < 0.3 and K < E) else "uniform"
+        budget = int(rng.choice([1, 2, 3, 5, 16, 24, 48]))
+        cases.append((T, H, E, K, mask, routing, budget, 300 + i))
+    return cases
+
+
+@pytest.mark.parametrize("T,H,E,K,mask,routing,budget,seed", _fuzz_small_cases())
+def test_random_small_tables_both_call_forms(ep, T, H, E, K, mask, routing, budget, seed):
+    inp = _custom(T, H, E, K, seed=seed, mask=mask, routing=routing)
+    num_recv = int((inp.topk_idx >= 0).sum()) + 1
+    ref = oracle_path(inp, num_recv, 1.5)
+    assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget, fused=True), ref)
+    assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget), ref)
+
+
 @pytest.mark.parametrize("T,H,E,K,mask,routing,budget,seed", _fuzz_cases())
 def test_random_shapes(ep, T, H, E, K, mask, routing, budget, seed):
     inp = _custom(T, H, E, K, seed=seed, mask=mask, routing=routing)
