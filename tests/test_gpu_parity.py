@@ -426,6 +426,66 @@ def test_back_to_back_batches_share_buffers_on_one_stream(ep):
     ep.ep_set_launch_overlap(0)
 
 
+def test_layers_chained_through_layout_dispatch_on_one_stream(ep):
+    """Four MoE layers back to back on one stream with no host
+    synchronisation, each layer's combine output being the next layer's
+    input x (as in a model), through ep_layout_dispatch + ep_combine. With
+    launch overlap, a dispatch whose layout kernel precedes it issues its
+    first row loads before waiting for that kernel; x is then the previous
+    layer's combine output, complete only because the layout kernel waits
+    for it before it lets dispatch launch. Every layer's slots, rows and
+    output are compared with the oracle's chain, at the full budget (launch
+    overlap on), at 24 SMs (off) and at 24 SMs with it forced on."""
+    dev = torch.device("cuda:0")
+    T, H = 300, 2056
+    layers = [(64, 6, "uniform", 1.5), (256, 8, "zipf", 1.0), (16, 2, "uniform", 1.5),
+              (128, 1, "uniform", 1.0)]
+    first = _custom(T, H, layers[0][0], layers[0][1], seed=70)
+    routes = [_custom(T, 8, E, K, seed=71 + i, routing=r) for i, (E, K, r, _) in enumerate(layers)]
+    # the oracle's chain
+    x_bits = first.x_bits()
+    refs = []
+    for (E, K, _, sc), rt in zip(layers, routes):
+        o = _oracle()
+        counts, offsets, slot, st = o.layout(rt.topk_idx.numpy(), E)
+        recv_x, _, _ = o.dispatch(x_bits, slot, T * K, rt.topk_w.numpy(), fill=CANARY)
+        eo = bits(W.expert_standin(from_bits(recv_x), sc))
+        y = o.combine(eo, slot, rt.topk_w.numpy())
+        refs.append((slot, recv_x, y))
+        x_bits = y
+    s = torch.cuda.Stream()
+    try:
+        for b, mode in ((0, 0), (24, 0), (24, 1)):
+            ep.ep_set_num_sms(b)
+            ep.ep_set_launch_overlap(mode)
+            with torch.cuda.stream(s):
+                x = first.x.to(dev)
+                status = torch.zeros(1, dtype=torch.int32, device=dev)
+                outs = []
+                for (E, K, _, sc), rt in zip(layers, routes):
+                    idx, w = rt.topk_idx.to(dev), rt.topk_w.to(dev)
+                    counts = torch.empty(E, dtype=torch.int32, device=dev)
+                    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+                    slot = torch.full((T, K), -5, dtype=torch.int32, device=dev)
+                    recv = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+                    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+                    ep.ep_layout_dispatch(idx, E, x, counts, offsets, slot, recv, None, None, None,
+                                          status, s)
+                    eo = W.expert_standin(recv, sc)
+                    ep.ep_combine(eo, slot, w, y, status, s)
+                    outs.append((slot, recv, y))
+                    x = y
+            s.synchronize()
+            assert ep.ep_get_status(status) == ep.EP_OK
+            for i, ((slot, recv, y), (r_slot, r_recv, r_y)) in enumerate(zip(outs, refs)):
+                assert np.array_equal(slot.cpu().numpy(), r_slot), f"budget {b}, mode {mode}, layer {i}: slot"
+                assert np.array_equal(bits(recv), r_recv), f"budget {b}, mode {mode}, layer {i}: recv_x"
+                assert np.array_equal(bits(y), r_y), f"budget {b}, mode {mode}, layer {i}: y"
+    finally:
+        ep.ep_set_num_sms(0)
+        ep.ep_set_launch_overlap(0)
+
+
 @pytest.mark.parametrize("T,H,E,K", [
     (128, 7168, 256, 8),   # decode: one-block layout
     (2048, 2048, 64, 8),   # one thread-block cluster layout
