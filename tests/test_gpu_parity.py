@@ -486,6 +486,83 @@ def test_layers_chained_through_layout_dispatch_on_one_stream(ep):
         ep.ep_set_launch_overlap(0)
 
 
+def _stream_mix(n=12, seed=5151):
+    """Seeded heterogeneous batches: any table size up to 24K entries (every
+    layout launch shape but the largest), any row size, either call form."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.choice([1, 8, 64, 256, 1024, 4096]))
+        K = int(rng.integers(1, min(E, 8) + 1))
+        T = int(rng.integers(1, 3000))
+        H = 8 * int(rng.integers(1, 600))
+        mask = float(rng.choice([0.0, 0.0, 0.2]))
+        out.append((T, H, E, K, mask, bool(rng.random() < 0.5), 500 + i))
+    return out
+
+
+@functools.lru_cache(maxsize=1)
+def _stream_mix_inputs():
+    """Inputs and oracle results of _stream_mix(), computed once."""
+    res = []
+    for T, H, E, K, mask, fused, seed in _stream_mix():
+        inp = _custom(T, H, E, K, seed=seed, mask=mask)
+        num_recv = int((inp.topk_idx >= 0).sum()) + 1
+        res.append((inp, num_recv, oracle_path(inp, num_recv, 1.0)))
+    return res
+
+
+@pytest.mark.parametrize("budget,mode", [(0, 0), (24, 1), (5, 0)])
+def test_heterogeneous_batches_back_to_back(ep, budget, mode):
+    """Twelve unrelated batches (random sizes, layout launch shapes and call
+    forms, each with its own buffers) issued back to back on one stream with
+    no host synchronisation, with launch overlap (the default at the full
+    budget, forced at 24 SMs) and without it (5 SMs): each kernel may start
+    while a kernel of another shape finishes."""
+    dev = torch.device("cuda:0")
+    cases = _stream_mix()
+    prepared = _stream_mix_inputs()
+    refs, runs = [], []
+    s = torch.cuda.Stream()
+    try:
+        ep.ep_set_num_sms(budget)
+        ep.ep_set_launch_overlap(mode)
+        for (T, H, E, K, mask, fused, seed), (inp, num_recv, ref) in zip(cases, prepared):
+            refs.append(ref)
+            with torch.cuda.stream(s):
+                idx, w, x = inp.topk_idx.to(dev), inp.topk_w.to(dev), inp.x.to(dev)
+                counts = torch.empty(E, dtype=torch.int32, device=dev)
+                offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+                slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+                recv = torch.full((num_recv, H), CANARY, dtype=torch.int16,
+                                  device=dev).view(torch.bfloat16)
+                y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+                status = torch.zeros(1, dtype=torch.int32, device=dev)
+                if fused:
+                    ep.ep_layout_dispatch(idx, E, x, counts, offsets, slot, recv, None, None,
+                                          None, status, s)
+                else:
+                    nws = ep.ep_layout_workspace_bytes(T, K, E)
+                    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev) if nws else None
+                    ep.ep_get_dispatch_layout(idx, E, counts, offsets, slot, ws, status, s)
+                    ep.ep_dispatch(x, slot, recv, None, None, None, status, s)
+                ep.ep_combine(recv, slot, w, y, status, s)
+                runs.append((counts, offsets, slot, recv, y, status, ws if not fused else None))
+        s.synchronize()
+        for (T, H, E, K, mask, fused, seed), ref, (counts, offsets, slot, recv, y, status, _) in zip(
+                cases, refs, runs):
+            what = f"T={T} H={H} E={E} K={K} fused={fused}"
+            assert ep.ep_get_status(status) == ep.EP_OK, what
+            assert np.array_equal(counts.cpu().numpy(), ref.counts), what
+            assert np.array_equal(offsets.cpu().numpy(), ref.offsets), what
+            assert np.array_equal(slot.cpu().numpy(), ref.slot), what
+            assert np.array_equal(bits(recv), ref.recv_x), what
+            assert np.array_equal(bits(y), ref.y), what
+    finally:
+        ep.ep_set_num_sms(0)
+        ep.ep_set_launch_overlap(0)
+
+
 @pytest.mark.parametrize("T,H,E,K", [
     (128, 7168, 256, 8),   # decode: one-block layout
     (2048, 2048, 64, 8),   # one thread-block cluster layout
