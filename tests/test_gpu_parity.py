@@ -672,13 +672,41 @@ def test_fused_one_launch_warps_split_by_the_id_count(ep, T, H, E, K, budget):
     assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget, fused=True), ref)
 
 
-def test_fused_layout_dispatch_bad_ids(ep):
+@pytest.mark.parametrize("budget", [0, 3])
+def test_fused_layout_dispatch_bad_ids(ep, budget):
+    # budget 0: the layout kernel and dispatch (launches overlap); 3 SMs:
+    # the one-launch form
     inp = _custom(300, 64, 32, 4)
     idx = inp.topk_idx.clone()
     idx[5, 1] = 99
     idx[200, 0] = -4
     inp = dataclasses.replace(inp, topk_idx=idx.contiguous())
     ref = oracle_path(inp, 300 * 4, 1.0)
-    got = gpu_path(ep, inp, 300 * 4, ref.expert_out, fused=True)
+    got = gpu_path(ep, inp, 300 * 4, ref.expert_out, num_sms=budget, fused=True)
     assert got["status"] == ep.EP_ERR_BAD_EXPERT
     assert_parity(got, ref)
+
+
+@pytest.mark.parametrize("budget", [0, 3])
+def test_fused_layout_dispatch_receive_buffer_too_small(ep, budget):
+    """ep_layout_dispatch into a receive buffer of 100 rows for 128
+    entries: the rows that fit are written, the others reported."""
+    inp = _custom(64, 64, 4, 2)
+    ref = oracle_path(inp, 64 * 2, 1.0)
+    dev = torch.device("cuda:0")
+    ep.ep_set_num_sms(budget)
+    try:
+        counts = torch.empty(4, dtype=torch.int32, device=dev)
+        offsets = torch.empty(5, dtype=torch.int32, device=dev)
+        slot = torch.empty((64, 2), dtype=torch.int32, device=dev)
+        small = torch.zeros((100, 64), dtype=torch.bfloat16, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ep.ep_layout_dispatch(inp.topk_idx.to(dev), 4, inp.x.to(dev), counts, offsets, slot, small,
+                              status=status)
+        assert ep.ep_get_status(status) == ep.EP_ERR_BAD_SLOT
+        assert np.array_equal(slot.cpu().numpy(), ref.slot)
+        ok = ref.slot.reshape(-1) < 100
+        rows = ref.slot.reshape(-1)[ok]
+        assert np.array_equal(bits(small)[rows], ref.recv_x[rows])
+    finally:
+        ep.ep_set_num_sms(0)
