@@ -104,3 +104,41 @@ def test_noalloc_matches_oracle_on_consecutive_calls(ep):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     for wl in cases:
         _check(ep, wl, status, dev)
+
+
+def _random_tables(n=16, seed=909):
+    """Seeded tables of every layout launch shape (one block, one cluster,
+    cooperative, tile + finish) within the scratch limit, with masked
+    entries, in random order."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        E = int(rng.choice([1, 3, 64, 128, 300, 1024, 4096]))
+        K = int(rng.integers(1, min(E, 8) + 1))
+        T = int(rng.integers(1, 40000))
+        if T * K > 320000:
+            continue
+        wl = W.Workload(f"noalloc-rand-{len(out)}", T=T, H=8, E=E, K=K, seed=900 + len(out),
+                        mask_frac=float(rng.choice([0.0, 0.1])))
+        out.append(wl)
+    return out
+
+
+@pytest.mark.gpu
+def test_noalloc_random_tables_in_sequence(ep):
+    """Sixteen seeded tables through the no-allocation layout one after
+    another (whatever the previous call left in the scratch), each against
+    the oracle and the workspace call; tables over the scratch limit must be
+    refused before any device work."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for wl in _random_tables():
+        if ep.ep_layout_workspace_bytes(wl.T, wl.K, wl.E) > ep.EP_NOALLOC_SCRATCH_BYTES:
+            A = 0x10000
+            code = ep.lib.ep_get_dispatch_layout_noalloc(A, wl.T, wl.K, wl.E, A, A, A, None, None)
+            assert code == ep.EP_ERR_UNSUPPORTED
+            continue
+        _check(ep, wl, status, dev)
