@@ -50,6 +50,9 @@ namespace {
 #ifndef EP_DISPATCH_LOAD_NORMAL
 #define EP_DISPATCH_LOAD_NORMAL 0
 #endif
+#ifndef EP_DISPATCH_FILL_RING
+#define EP_DISPATCH_FILL_RING 1
+#endif
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr int kDispatchWarps = EP_DISPATCH_WARPS;
@@ -275,8 +278,13 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
                   a.x + t * static_cast<int64_t>(a.row_bytes) + off, bytes, bar, pol_load);
     };
 
+    // Loads issued before the ring starts: P, or the whole ring (NS) when
+    // the kernel has to wait before its first store anyway (the fused
+    // layout, or a layout kernel it overlaps) and no stage is being stored.
+    const bool fill_ring = EP_DISPATCH_FILL_RING && (FUSED || a.x_ready != 0);
+    const int64_t prefilled = fill_ring ? (n < NS ? n : NS) : (n < P ? n : P);
     auto first_loads = [&]() {
-        for (int64_t j = 0; j < P && j < n; ++j) issue_load(j);
+        for (int64_t j = 0; j < prefilled; ++j) issue_load(j);
     };
     // Every global-memory access waits for the previous kernel on the stream
     // (programmatic dependent launch), except the first row loads when x is
@@ -339,7 +347,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
 
         // Refill: the stage of unit j+P was last used by unit j+P-NS; its
         // stores must have finished reading shared memory.
-        if (j + P < n) {
+        if (j + P < n && j + P >= prefilled) {
             if (leader) bulk_wait_read<NS - P - 1>();
             issue_load(j + P);
         }
@@ -351,7 +359,10 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
         if (!ok) {
             if (leader) {
                 set_status(a.status, EP_ERR_TIMEOUT);
-                mbar_drain_bounded<NS>(bar0, j, j + P < n ? j + P : n - 1);
+                const int64_t last_issued = (j + P < n ? j + P : n - 1) > prefilled - 1
+                                                ? (j + P < n ? j + P : n - 1)
+                                                : prefilled - 1;
+                mbar_drain_bounded<NS>(bar0, j, last_issued);
             }
             break;
         }
