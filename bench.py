@@ -190,6 +190,13 @@ class Step:
         self.b.idx.copy_(inp.topk_idx)
         self.b.w.copy_(inp.topk_w)
         self.layout_launches = ep.ep_layout_launches(self.T, self.K, self.E)
+        # x larger than 8 MB is rotated over four device copies, so that no
+        # dispatch finds the previous call's x in L2 (the rotated copies
+        # together exceed it); decode-size x stays warm, as in a decode loop
+        self.x_ring = [self.b.x]
+        if self.b.x.numel() * 2 > (8 << 20):
+            self.x_ring += [self.b.x.clone() for _ in range(3)]
+        self._xi = 0
         # the experts between dispatch and combine are a fixed stand-in
         self.layout(self.b)
         self.dispatch(self.b)
@@ -200,15 +207,22 @@ class Step:
         self.ep.ep_get_dispatch_layout(b.idx, self.E, b.counts, b.offsets, b.slot, b.ws,
                                        b.status, stream)
 
+    def next_x(self, b: Buffers) -> torch.Tensor:
+        if b is not self.b:
+            return b.x
+        x = self.x_ring[self._xi]
+        self._xi = (self._xi + 1) % len(self.x_ring)
+        return x
+
     def dispatch(self, b: Buffers, stream=None):
-        self.ep.ep_dispatch(b.x, b.slot, b.recv_x, None, None, None, b.status, stream)
+        self.ep.ep_dispatch(self.next_x(b), b.slot, b.recv_x, None, None, None, b.status, stream)
 
     def combine(self, b: Buffers, stream=None):
         self.ep.ep_combine(self.expert_out, b.slot, b.w, b.y, b.status, stream)
 
     def layout_dispatch(self, b: Buffers, stream=None):
-        self.ep.ep_layout_dispatch(b.idx, self.E, b.x, b.counts, b.offsets, b.slot, b.recv_x,
-                                   None, None, None, b.status, stream)
+        self.ep.ep_layout_dispatch(b.idx, self.E, self.next_x(b), b.counts, b.offsets, b.slot,
+                                   b.recv_x, None, None, None, b.status, stream)
 
     def run(self, b: Buffers, stream=None):
         self.layout(b, stream)
@@ -1514,8 +1528,9 @@ def main():
                 "num_sms": sms_all,
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                 "accumulate": "fp32 (combine)",
-                "l2": "no flush: inputs larger than L2 (x 58.7 MB is re-read after "
-                      "~1 GB of other traffic per step; recv/expert_out 470 MB each)",
+                "l2": "no flush: inputs larger than L2 (recv/expert_out 470 MB each; x, "
+                      "58.7 MB, rotated over four device copies, 235 MB, so no step reads "
+                      "the previous step's x from L2)",
             },
             "hbm": {
                 "all_sms": s_all,

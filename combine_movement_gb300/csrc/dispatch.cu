@@ -53,9 +53,18 @@ namespace {
 #ifndef EP_DISPATCH_FILL_RING
 #define EP_DISPATCH_FILL_RING 1
 #endif
+#ifndef EP_DISPATCH_L2_PREFETCH
+#define EP_DISPATCH_L2_PREFETCH 1
+#endif
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr int kDispatchWarps = EP_DISPATCH_WARPS;
+// Units beyond the filled ring that a warp prefetches into L2 while the
+// layout holds back its first store (full budget only).
+#ifndef EP_DISPATCH_L2_UNITS
+#define EP_DISPATCH_L2_UNITS 4
+#endif
+constexpr int64_t kL2PrefetchUnits = EP_DISPATCH_L2_UNITS;
 
 // Bytes reserved in front of the stages for the mbarriers (8 B per stage per
 // warp), rounded up so every stage starts 128-byte aligned.
@@ -285,6 +294,27 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     const int64_t prefilled = fill_ring ? (n < NS ? n : NS) : (n < P ? n : P);
     auto first_loads = [&]() {
         for (int64_t j = 0; j < prefilled; ++j) issue_load(j);
+#if EP_DISPATCH_L2_PREFETCH
+        // While the layout still holds back the first store, the warp's
+        // next kL2PrefetchUnits rows are brought into L2 too (evict-last, so
+        // the receive rows streaming through L2 do not push them out
+        // first). More than that crowds L2 for the rest of the kernel.
+        if (fill_ring && leader && a.l2_prefetch != 0) {
+            const uint64_t pol_keep = policy_evict_last();
+            int64_t pt = lt;
+            uint32_t pc = lc;
+            const int64_t end = n < prefilled + kL2PrefetchUnits ? n : prefilled + kL2PrefetchUnits;
+            for (int64_t j = prefilled; j < end; ++j) {
+                const uint32_t off = pc * a.chunk_bytes;
+                bulk_prefetch_l2(a.x + pt * static_cast<int64_t>(a.row_bytes) + off,
+                                 min(a.chunk_bytes, a.row_bytes - off), pol_keep);
+                if (++pc == a.n_chunks) {
+                    pc = 0;
+                    ++pt;
+                }
+            }
+        }
+#endif
     };
     // Every global-memory access waits for the previous kernel on the stream
     // (programmatic dependent launch), except the first row loads when x is

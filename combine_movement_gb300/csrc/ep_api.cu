@@ -326,6 +326,7 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
                                status, smem_optin, 0, n, false, s);
             if (st != EP_OK) return st;
             a.x_ready = 1;
+            a.l2_prefetch = n >= sm_count ? 1 : 0;
             return from_cuda(ep::launch_dispatch(a, n, smem_optin, s));
         }
     }

@@ -118,6 +118,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ uint64_t policy_evict_normal() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
@@ -146,6 +152,14 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_
         "cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
         "r"(src_smem), "r"(bytes), "l"(policy)
         : "memory");
+}
+
+// Bring `bytes` of global memory into L2 (no shared memory, no completion
+// to wait for); a hint only.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+                 "r"(bytes), "l"(policy)
+                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() {
