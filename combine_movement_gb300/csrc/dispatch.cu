@@ -322,6 +322,27 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     // ep_layout_dispatch precedes this launch); they then overlap it.
     const bool early = !FUSED && a.x_ready != 0;
     if (early) first_loads();
+#if EP_DISPATCH_L2_PREFETCH
+    // Without x_ready the kernel before this one may still be writing x, so
+    // nothing may be copied into shared memory yet; bringing the first
+    // rows into L2 is safe (L2 is coherent: a later write updates the
+    // line) and uses the time this kernel would otherwise only wait.
+    if (!FUSED && !early && a.l2_prefetch != 0 && leader) {
+        const uint64_t pol_keep = policy_evict_last();
+        int64_t pt = lt;
+        uint32_t pc = lc;
+        const int64_t end = n < prefilled + kL2PrefetchUnits ? n : prefilled + kL2PrefetchUnits;
+        for (int64_t j = 0; j < end; ++j) {
+            const uint32_t off = pc * a.chunk_bytes;
+            bulk_prefetch_l2(a.x + pt * static_cast<int64_t>(a.row_bytes) + off,
+                             min(a.chunk_bytes, a.row_bytes - off), pol_keep);
+            if (++pc == a.n_chunks) {
+                pc = 0;
+                ++pt;
+            }
+        }
+    }
+#endif
     griddep_wait();
     griddep_launch_dependents();
 

@@ -287,6 +287,8 @@ ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const in
     st = plan_dispatch(&a, x, T, H, K, slot, topk_w, num_recv, recv_x, recv_w, recv_src, status,
                        smem_optin, 0, n, false, s);
     if (st != EP_OK) return st;
+    // an early-started kernel brings its first rows into L2 while it waits
+    a.l2_prefetch = (n >= sm_count && ep::launch_overlap_allowed(s)) ? 1 : 0;
     return from_cuda(ep::launch_dispatch(a, n, smem_optin, s));
 }
 

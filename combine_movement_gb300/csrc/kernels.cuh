@@ -85,13 +85,13 @@ struct DispatchArgs {
     // before by ep_layout_dispatch, which never writes x), so the first row
     // loads may go out before the kernel waits for its predecessor.
     int x_ready;
-    // 1: while the first store still waits for the layout kernel, also
-    // bring the warp's next rows into L2. Set by ep_layout_dispatch's
-    // two-launch form at the full SM budget, where dispatch is bound by
-    // DRAM (DeepSeek-V3 step -3.2 us); on a partial budget the SMs' own
-    // write path bounds it, and in the one-launch form (tables that need a
-    // workspace, whose per-CTA layout is long) the prefetched rows only
-    // crowd L2 (+1-2 %).
+    // 1: while the first store still waits for the kernel before it (the
+    // layout kernel, when launches overlap), bring the warp's next rows
+    // into L2. Set at the full SM budget with launch overlap in effect,
+    // where dispatch is bound by DRAM (DeepSeek-V3 step -3.2 us); on a
+    // partial budget the SMs' own write path bounds it, and in the
+    // one-launch form (tables that need a workspace, whose per-CTA layout
+    // is long) the prefetched rows only crowd L2 (+1-2 %).
     int l2_prefetch;
 };
 
