@@ -192,8 +192,11 @@ EP_API ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K,
  *    step takes 29.4 us with it, 33.4 us with the separate calls).
  *  - Otherwise, when the layout needs no workspace (at most 65,536 entries
  *    at E <= 256): the layout kernel and the dispatch kernel, with
- *    dispatch's first row loads issued while the layout runs (safe because
- *    this call launched that layout kernel itself, which never writes x).
+ *    dispatch's first row loads (its whole ring; at the full SM budget also
+ *    the next rows, into L2) issued while the layout runs (safe because
+ *    this call launched that layout kernel itself, which never writes x):
+ *    on GB300 the DeepSeek-V3 prefill step (T=4096 top-8, H=7168) takes
+ *    0.173 ms with it and 0.177 ms with the separate calls.
  *  - Larger tables fall back to the one-launch form, whose cost grows with
  *    T*K per CTA; call the two functions separately for those.
  * Arguments as in those two calls; T == 0 still writes zero counts and
