@@ -384,7 +384,9 @@ def time_e2e(step: Step, inp: W.Inputs, steps: int, warmup: int) -> dict:
     hidx = inp.topk_idx.pin_memory()
     hw = inp.topk_w.pin_memory()
     hy = [torch.empty(step.b.y.shape, dtype=step.b.y.dtype).pin_memory() for _ in range(2)]
-    bufs = [step.b, Buffers(step.ep, step.wl, dev)]
+    # two buffer sets of their own (step.b's x is rotated over copies the
+    # host copy would not reach)
+    bufs = [Buffers(step.ep, step.wl, dev) for _ in range(2)]
     h2d = hx.numel() * hx.element_size() + hidx.numel() * 8 + hw.numel() * 4
     d2h = hy[0].numel() * hy[0].element_size()
     s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
