@@ -87,11 +87,17 @@ def oracle_path(inp: W.Inputs, num_recv: int, expert_scale: float) -> Ref:
 
 
 def gpu_path(ep, inp: W.Inputs, num_recv: int, expert_out: np.ndarray, num_sms: int = 0,
-             stream=None, fused: bool = False):
+             stream=None, fused: bool = False, idx_shifted: bool = False):
     dev = torch.device("cuda:0")
     E = inp.wl.E
     ep.ep_set_num_sms(num_sms)
     idx = inp.topk_idx.to(dev)
+    if idx_shifted:
+        # the same table starting 8 bytes past a 16-byte boundary
+        buf = torch.empty(idx.numel() + 1, dtype=torch.int64, device=dev)
+        buf[1:] = idx.reshape(-1)
+        idx = buf[1:].view(idx.shape)
+        assert idx.data_ptr() % 16 == 8
     w = inp.topk_w.to(dev)
     x = inp.x.to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -670,6 +676,41 @@ def test_fused_one_launch_warps_split_by_the_id_count(ep, T, H, E, K, budget):
     num_recv = T * K + 1
     ref = oracle_path(inp, num_recv, 1.5)
     assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget, fused=True), ref)
+
+
+@pytest.mark.parametrize("T,H,E,K,budget,mask,bad,shifted", [
+    (128, 256, 128, 8, 8, 0.0, False, False),   # 1024 entries, 128 per CTA, kept in shared memory
+    (128, 7168, 575, 8, 24, 0.05, True, False), # decode-size table, three-chunk rows, odd E
+    (256, 64, 256, 4, 24, 0.1, True, True),     # masked and out-of-range ids, shifted table
+    (205, 64, 256, 5, 24, 0.1, True, True),     # 1025 entries
+    (7, 40, 5, 3, 2, 0.0, True, True),          # 21 entries: first id read on its own
+    (11, 40, 5, 2, 2, 0.0, False, True),        # first id and odd last id read on their own
+    (1, 8, 1, 1, 1, 0.0, False, False),         # one entry
+    (100, 512, 4096, 8, 16, 0.05, True, False), # 4096 experts, the last one's id
+])
+def test_fused_one_launch_edges(ep, T, H, E, K, budget, mask, bad, shifted):
+    """The one-launch ep_layout_dispatch (small tables on a partial budget:
+    every CTA lays out the whole table before its ring): tables of 1 to
+    1025 entries, with masked entries, out-of-range ids, the last expert's
+    id, and an id table that starts 8 bytes past a 16-byte boundary (its
+    first id then read on its own)."""
+    inp = _custom(T, H, E, K, seed=T * 31 + budget, mask=mask)
+    idx = inp.topk_idx.clone()
+    idx[0, 0] = E - 1
+    if bad and T >= 3:
+        idx[1, 0] = E + 3
+        idx[2, K - 1] = -9
+    inp = dataclasses.replace(inp, topk_idx=idx.contiguous())
+    num_recv = T * K + 2
+    ref = oracle_path(inp, num_recv, 1.25)
+    got = gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget, fused=True,
+                   idx_shifted=shifted)
+    if bad and T >= 3:
+        assert got["status"] == ep.EP_ERR_BAD_EXPERT
+    assert_parity(got, ref)
+    if shifted:  # the layout kernel reads the shifted table too
+        assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget,
+                               idx_shifted=True), ref)
 
 
 @pytest.mark.parametrize("budget", [0, 3])
