@@ -687,6 +687,9 @@ def decode_latency(ep, dev, budgets=(16, 24, 0), ceilings: dict | None = None) -
             "warm_us": round(warm, 2), "cold_us": round(cold, 2),
             "cold_gbs": round((ab["dispatch"] + ab["combine"]) / (cold * 1e-6) / 1e9, 1),
             "fused_warm_us": round(fwarm, 2), "fused_cold_us": round(fcold, 2),
+            # the same two warm steps net of what an empty launch measures
+            # between the same events (event records and one launch)
+            "warm_net_us": round(warm - overhead, 2), "fused_warm_net_us": round(fwarm - overhead, 2),
             "graph_warm_us": round(gwarm, 2),
             "launch_overlap_forced_warm_us": round(owarm, 2),
             # steps issued back to back from the host (no spin in between):
@@ -722,7 +725,10 @@ def decode_latency(ep, dev, budgets=(16, 24, 0), ceilings: dict | None = None) -
                     pf = time_call(lambda: step.run_fused(step.b), 200)
                     pb = back_to_back(lambda: step.run(step.b))
                 entry["partition"] = {"sms": n_part, "warm_us": round(pw, 2),
-                                      "fused_warm_us": round(pf, 2), "back_to_back_us": round(pb, 2)}
+                                      "fused_warm_us": round(pf, 2),
+                                      "warm_net_us": round(pw - overhead, 2),
+                                      "fused_warm_net_us": round(pf - overhead, 2),
+                                      "back_to_back_us": round(pb, 2)}
             except Exception as e:  # noqa: BLE001 - reported in the line
                 entry["partition"] = {"unavailable": str(e)[:200]}
         c = (ceilings or {}).get(n)
