@@ -247,11 +247,12 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     }
     __syncwarp();
 
-    const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
+    // this launch's units, split evenly over its warps
+    const int64_t units = a.unit_count;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
-    const int64_t u0 = split_begin(units, gw, nw_total);
-    const int64_t n = split_begin(units, gw + 1, nw_total) - u0;
+    const int64_t u0 = a.unit_base + split_begin(units, gw, nw_total);
+    const int64_t n = a.unit_base + split_begin(units, gw + 1, nw_total) - u0;
 
     // L2 policies: x is read once (evict first); the receive rows are
     // written once and next read by the experts (normal).
@@ -343,7 +344,9 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
         }
     }
 #endif
-    griddep_wait();
+    // (A tail launch's CTAs skip the wait, all but its last; see
+    // DispatchArgs::tail.)
+    if (!a.tail || blockIdx.x == gridDim.x - 1) griddep_wait();
     griddep_launch_dependents();
 
     // The fused kernel's entries: the CTA's slots stay in shared memory
@@ -528,6 +531,23 @@ constexpr int kPrefetch = EP_DISPATCH_PREFETCH;
 #endif
 constexpr int kSharedStages = EP_DISPATCH_SHARED_STAGES;
 static_assert(kSharedStages > kPrefetch, "need more stages than loads in flight");
+// Warps of a tail CTA (DispatchArgs::tail_units), one unit each: 2 where
+// rows are cut into chunks, 4 where a row is one chunk. Measured with the
+// combine that follows (step back to back): DeepSeek-V3 prefill (two 7 KB
+// chunks per row) 162.8 / 165.3 / 174.1 us with 2 / 3 / 4 warps, skewed
+// Zipf (8 KB rows, one chunk) 157.3 / 146.6 / 145.9 us with 2 / 3 / 4.
+#ifndef EP_DISPATCH_TAIL_WARPS
+#define EP_DISPATCH_TAIL_WARPS 0
+#endif
+int tail_warps(const DispatchArgs& a) {
+    if (EP_DISPATCH_TAIL_WARPS > 0) return EP_DISPATCH_TAIL_WARPS;
+    return a.n_chunks >= 2 ? 2 : 4;
+}
+// 1: a tail CTA asks for more shared memory than an SM has beside a ring
+// CTA, so it never shares an SM with one.
+#ifndef EP_DISPATCH_TAIL_EXCLUSIVE
+#define EP_DISPATCH_TAIL_EXCLUSIVE 1
+#endif
 
 }  // namespace
 
@@ -541,11 +561,47 @@ cudaError_t launch_ring(const DispatchArgs& a, int num_sms, cudaStream_t stream)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(request));
     if (err != cudaSuccess) return err;
-    const int64_t units = a.T * static_cast<int64_t>(a.n_chunks);
-    int64_t ctas_needed = (units + kDispatchWarps - 1) / kDispatchWarps;
+    DispatchArgs ring = a;
+    ring.unit_count = a.unit_count - a.tail_units;
+    const int64_t ctas_needed = (ring.unit_count + kDispatchWarps - 1) / kDispatchWarps;
     const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
     if (grid <= 0) return cudaSuccess;
-    return launch_dependent(kern, grid, kDispatchWarps * 32, request, stream, a, FusedLayoutArgs{});
+    err = launch_dependent(kern, grid, kDispatchWarps * 32, request, stream, ring, FusedLayoutArgs{});
+    if (err != cudaSuccess || a.tail_units <= 0) return err;
+    // The tail: small CTAs of tw warps, one unit per warp, on the
+    // same ring shape, each asking for more shared memory than an SM has
+    // beside a ring CTA (DispatchArgs::tail_units).
+    const int tw = tail_warps(a);
+    DispatchArgs tail = a;
+    tail.unit_base = a.unit_base + ring.unit_count;
+    tail.unit_count = a.tail_units;
+    tail.tail = 1;
+    tail.x_ready = 0;
+    tail.l2_prefetch = 0;
+    int dev = 0, per_sm = 0, reserved = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+        cudaSuccess)
+        return err;
+    if ((err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+        cudaSuccess)
+        return err;
+    const size_t need = static_cast<size_t>(barrier_region(NS, tw)) +
+                        static_cast<size_t>(tw) * NS * a.stage_bytes;
+    // free beside a ring CTA, less the tail CTA's own reserved bytes
+    const long long spare = static_cast<long long>(per_sm) - static_cast<long long>(request) -
+                            2ll * reserved;
+    size_t tail_request = need;
+    if (EP_DISPATCH_TAIL_EXCLUSIVE && spare >= 0 && static_cast<size_t>(spare) + 128 > tail_request)
+        tail_request = (static_cast<size_t>(spare) + 128) & ~static_cast<size_t>(127);
+    auto tkern = dispatch_kernel<NS, kPrefetch, false>;
+    if (tail_request > request &&
+        (err = cudaFuncSetAttribute(tkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(tail_request))) != cudaSuccess)
+        return err;
+    const int tail_grid = static_cast<int>((a.tail_units + tw - 1) / tw);
+    return launch_dependent(tkern, tail_grid, tw * 32, tail_request, stream, tail,
+                            FusedLayoutArgs{});
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, int num_sms, int smem_optin,

@@ -93,6 +93,26 @@ struct DispatchArgs {
     // one-launch form (tables that need a workspace, whose per-CTA layout
     // is long) the prefetched rows only crowd L2 (+1-2 %).
     int l2_prefetch;
+    // This launch moves units [unit_base, unit_base + unit_count) of the
+    // T * n_chunks (token, chunk) units.
+    int64_t unit_base;
+    int64_t unit_count;
+    // Units the host gives to a tail launch (launch_dispatch), 0 for none.
+    // At the full budget, with launches overlapping, the SMs do not move
+    // bytes equally fast: under the same load some finish an equal share of
+    // the units 25-35 % later than others (by SM, the same pattern launch
+    // after launch). So the ring launch takes all but the last tail_units,
+    // split evenly, and a second launch of many small CTAs (kTailWarps
+    // warps, one unit each) takes the rest; those CTAs need more shared
+    // memory than an SM has beside a ring CTA, so each starts only on an SM
+    // whose ring CTA has finished, and the SMs that finish first take most
+    // of the tail (the block scheduler serves as the work queue).
+    int64_t tail_units;
+    // 1 in the tail launch: its CTAs start without waiting for the ring
+    // launch (they only read what the ring launch read, which was complete
+    // before the ring launch let them launch); its last CTA waits for the
+    // ring launch to complete, so the tail launch completes after it.
+    int tail;
 };
 
 // Routing inputs and layout outputs of the fused layout + dispatch kernel.

@@ -72,6 +72,10 @@ def _load() -> ctypes.CDLL:
     lib.ep_set_launch_overlap.restype = i32
     lib.ep_get_launch_overlap.argtypes = []
     lib.ep_get_launch_overlap.restype = i32
+    lib.ep_set_dispatch_tail.argtypes = [i32]
+    lib.ep_set_dispatch_tail.restype = i32
+    lib.ep_get_dispatch_tail.argtypes = []
+    lib.ep_get_dispatch_tail.restype = i32
     lib.ep_num_sms_in_effect.argtypes = []
     lib.ep_num_sms_in_effect.restype = i32
     lib.ep_layout_workspace_bytes.argtypes = [i64, i32, i32]
@@ -82,6 +86,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_dispatch_ring_stages.argtypes = []
     lib.ep_dispatch_ring_stages.restype = i32
     lib.ep_dispatch_chunk_bytes.restype = i64
+    lib.ep_dispatch_launches.argtypes = [i64, i64, i32, p]
+    lib.ep_dispatch_launches.restype = i32
     lib.ep_get_dispatch_layout.argtypes = [p, i64, i32, i32, p, p, p, p, sz, p, p]
     lib.ep_get_dispatch_layout.restype = i32
     lib.ep_dispatch.argtypes = [p, i64, i64, i32, p, p, i64, p, p, p, p, p]
@@ -163,6 +169,14 @@ def ep_get_launch_overlap() -> int:
     return lib.ep_get_launch_overlap()
 
 
+def ep_set_dispatch_tail(percent: int) -> int:
+    return lib.ep_set_dispatch_tail(int(percent))
+
+
+def ep_get_dispatch_tail() -> int:
+    return lib.ep_get_dispatch_tail()
+
+
 def ep_num_sms_in_effect() -> int:
     return lib.ep_num_sms_in_effect()
 
@@ -181,6 +195,10 @@ def ep_dispatch_chunk_bytes(T: int, H: int, K: int) -> int:
 
 def ep_dispatch_ring_stages() -> int:
     return int(lib.ep_dispatch_ring_stages())
+
+
+def ep_dispatch_launches(T: int, H: int, K: int, stream=None) -> int:
+    return int(lib.ep_dispatch_launches(T, H, K, _stream(stream)))
 
 
 def ep_status_string(code: int) -> str:

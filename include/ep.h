@@ -126,6 +126,13 @@ EP_API int ep_get_num_sms(void);
 EP_API int ep_set_launch_overlap(int mode);
 EP_API int ep_get_launch_overlap(void);
 
+/* Percentage (0 to 90, default 30) of a dispatch's (token, chunk) units
+ * that go to its tail launch where it makes one (ep_dispatch_launches);
+ * 0 keeps every dispatch to one persistent launch. Process-wide. Returns the
+ * stored value, or -1 (and changes nothing) outside that range. */
+EP_API int ep_set_dispatch_tail(int percent);
+EP_API int ep_get_dispatch_tail(void);
+
 /* The number of SMs dispatch/combine will use on the current device: the
  * budget clamped to [1, SM count]. Returns -1 if the device can't be queried. */
 EP_API int ep_num_sms_in_effect(void);
@@ -153,6 +160,22 @@ EP_API int64_t ep_dispatch_chunk_bytes(int64_t T, int64_t H, int K);
  * faster with the kernels overlapping), else 4. For measurements that model
  * the ring. */
 EP_API int ep_dispatch_ring_stages(void);
+
+/* Kernel launches one ep_dispatch call makes for these sizes on `stream`
+ * (NULL: the legacy default stream) at the current SM budget and
+ * launch-overlap mode: 2 when it splits the rows between a persistent launch
+ * and a tail launch, else 1; the dispatch part of ep_layout_dispatch in its
+ * two-launch form does the same. The split is made on the whole GPU, while
+ * launches overlap, for calls of at least 192 MB of receive rows and K >= 2
+ * (and a tail percentage above 0, ep_set_dispatch_tail). There, under one
+ * load, some SMs move an equal share 25-35 % later than others (the same SMs
+ * launch after launch), so the persistent launch takes 70 % of the (token,
+ * chunk) units, split evenly, and the tail launch's
+ * small CTAs take the rest, each starting only on an SM whose persistent CTA
+ * has finished: the SMs that finish first take most of the tail. For
+ * accounting in measurements; -1 for invalid sizes or when the device
+ * cannot be queried. */
+EP_API int ep_dispatch_launches(int64_t T, int64_t H, int K, void* stream);
 
 /* Layout (per-expert histogram, exclusive prefix sums and per-(token,k)
  * destination slot).
@@ -184,7 +207,11 @@ EP_API ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, in
  *   recv_x     bf16 [num_recv][H] out
  *   recv_w     fp32 [num_recv] out, nullable: recv_w[slot[t,k]] = topk_w[t,k]
  *   recv_src   int32 [num_recv] out, nullable: recv_src[slot[t,k]] = t*K + k
- * Rows of recv_x no (t,k) maps to are left untouched. */
+ * Rows of recv_x no (t,k) maps to are left untouched. One persistent CTA per
+ * SM of the budget, the (token, chunk) units split evenly over its warps;
+ * on the whole GPU, with launches overlapping, calls of at least 192 MB of
+ * receive rows (K >= 2) hand the last 30 % of the units to a second launch
+ * of small CTAs (ep_dispatch_launches). */
 EP_API ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K,
                         const int32_t* slot, const float* topk_w, int64_t num_recv,
                         uint16_t* recv_x, float* recv_w, int32_t* recv_src,

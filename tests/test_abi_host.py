@@ -94,6 +94,26 @@ def test_layout_launch_counts(ep):
     assert ep.ep_layout_launches(10, 33, 8) == -1
 
 
+def test_dispatch_tail_percentage_round_trip(ep):
+    before = ep.ep_get_dispatch_tail()
+    try:
+        assert before == 30
+        assert ep.ep_set_dispatch_tail(0) == 0 and ep.ep_get_dispatch_tail() == 0
+        assert ep.ep_set_dispatch_tail(90) == 90
+        assert ep.ep_set_dispatch_tail(91) == -1 and ep.ep_get_dispatch_tail() == 90
+        assert ep.ep_set_dispatch_tail(-1) == -1 and ep.ep_get_dispatch_tail() == 90
+    finally:
+        ep.ep_set_dispatch_tail(before)
+
+
+def test_dispatch_launches_rejects_invalid_sizes(ep):
+    # checked before the device is queried (no GPU needed)
+    assert ep.lib.ep_dispatch_launches(4096, 7166, 8, None) == -1   # H % 8 != 0
+    assert ep.lib.ep_dispatch_launches(4096, 7168, 33, None) == -1  # K above the limit
+    assert ep.lib.ep_dispatch_launches(-1, 7168, 8, None) == -1
+    assert ep.lib.ep_dispatch_launches(0, 7168, 8, None) == 0       # nothing to launch
+
+
 def test_dispatch_chunk_bytes_rejects_invalid_sizes(ep):
     assert ep.ep_dispatch_chunk_bytes(4096, 7166, 8) == -1   # H % 8 != 0
     assert ep.ep_dispatch_chunk_bytes(4096, 7168, 33) == -1  # K above the limit

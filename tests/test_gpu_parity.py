@@ -678,6 +678,59 @@ def test_fused_one_launch_warps_split_by_the_id_count(ep, T, H, E, K, budget):
     assert_parity(gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=budget, fused=True), ref)
 
 
+@pytest.mark.parametrize("T,H,E,K,mask,routing,short", [
+    (16384, 7168, 256, 2, 0.1, "uniform", 0),   # K = 2, masked
+    (6144, 7176, 64, 3, 0.0, "uniform", 0),     # 14352-byte rows (a ragged last chunk)
+    (2100, 6144, 32, 8, 0.25, "zipf", 0),       # just over the size limit (206 MB)
+    (4096, 7168, 256, 8, 0.0, "uniform", 100),  # receive buffer 100 rows short
+])
+def test_dispatch_tail_launch(ep, T, H, E, K, mask, routing, short):
+    """At the full budget, with launches overlapping, a dispatch of at least
+    192 MB of receive rows is two launches: a persistent ring over the first
+    70 % of the (token, chunk) units, then a tail of small CTAs over the rest
+    that start on SMs whose ring CTA has finished. Every row must come out
+    as the oracle's, through ep_dispatch and ep_layout_dispatch, with masked
+    entries, skewed routing, a ragged last chunk, an odd number of tail
+    units and rows beyond the receive buffer (reported, not written)."""
+    inp = _custom(T, H, E, K, seed=T + K, mask=mask, routing=routing)
+    R_valid = int((inp.topk_idx >= 0).sum())
+    ref = oracle_path(inp, R_valid, 1.0)   # the oracle gets room for every row
+    num_recv = R_valid - short
+    ep.ep_set_num_sms(0)
+    assert ep.ep_dispatch_launches(T, H, K) == 2
+    for fused in (False, True):
+        got = gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=0, fused=fused)
+        if short:
+            assert got["status"] == ep.EP_ERR_BAD_SLOT
+            flat = ref.slot.reshape(-1)
+            rows = flat[(flat >= 0) & (flat < num_recv)]
+            assert np.array_equal(got["slot"], ref.slot)
+            assert np.array_equal(got["recv_x"][rows], ref.recv_x[rows])
+        else:
+            assert_parity(got, ref)
+
+
+def test_dispatch_launch_counts(ep):
+    """One launch wherever the tail does not apply: decode-size batches, a
+    partial SM budget, launch overlap switched off."""
+    ep.ep_set_num_sms(0)
+    assert ep.ep_dispatch_launches(4096, 7168, 8) == 2
+    assert ep.ep_dispatch_launches(128, 7168, 8) == 1
+    assert ep.ep_dispatch_launches(1024, 7168, 8) == 1     # 117 MB of rows
+    assert ep.ep_dispatch_launches(16384, 7168, 1) == 1    # K = 1
+    mode = ep.ep_get_launch_overlap()
+    try:
+        ep.ep_set_launch_overlap(2)
+        assert ep.ep_dispatch_launches(4096, 7168, 8) == 1
+    finally:
+        ep.ep_set_launch_overlap(mode)
+    try:
+        ep.ep_set_num_sms(24)
+        assert ep.ep_dispatch_launches(4096, 7168, 8) == 1
+    finally:
+        ep.ep_set_num_sms(0)
+
+
 @pytest.mark.parametrize("T,H,E,K,budget,mask,bad,shifted", [
     (128, 256, 128, 8, 8, 0.0, False, False),   # 1024 entries, 128 per CTA, kept in shared memory
     (128, 7168, 575, 8, 24, 0.05, True, False), # decode-size table, three-chunk rows, odd E
