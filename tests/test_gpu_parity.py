@@ -710,6 +710,63 @@ def test_dispatch_tail_launch(ep, T, H, E, K, mask, routing, short):
             assert_parity(got, ref)
 
 
+@pytest.mark.parametrize("graph", [False, True])
+def test_combine_reads_the_rows_of_both_dispatch_launches(ep, graph):
+    """Combine launched right after a two-launch dispatch (ring + tail, the
+    whole GPU, launches overlapping) and reading the receive rows
+    themselves: it must find the rows of both launches, which holds because
+    the tail launch completes after the ring (its last CTA waits for it), so
+    combine's wait for its predecessor covers both. Eagerly and replayed
+    from a CUDA graph (the programmatic launches captured as such)."""
+    T, H, E, K = 2100, 6144, 32, 8
+    inps = [_custom(T, H, E, K, seed=60 + i) for i in range(2)]
+    refs = [oracle_path(inp, T * K, 1.0) for inp in inps]   # stand-in x1.0: the rows themselves
+    dev = torch.device("cuda:0")
+    ep.ep_set_num_sms(0)
+    assert ep.ep_dispatch_launches(T, H, K) == 2
+    idx = inps[0].topk_idx.to(dev).clone()
+    w = inps[0].topk_w.to(dev).clone()
+    x = inps[0].x.to(dev).clone()
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    recv = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(stream):
+        ep.ep_layout_dispatch(idx, E, x, counts, offsets, slot, recv, None, None, None,
+                              status, stream)
+        ep.ep_combine(recv, slot, w, y, status, stream)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step(s)
+    torch.cuda.synchronize()
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(torch.cuda.current_stream())
+    for inp, ref in zip(inps, refs):
+        idx.copy_(inp.topk_idx)
+        w.copy_(inp.topk_w)
+        x.copy_(inp.x)
+        recv.fill_(0)
+        y.fill_(0)
+        torch.cuda.synchronize()
+        if g is not None:
+            g.replay()
+        else:
+            with torch.cuda.stream(s):
+                step(s)
+        torch.cuda.synchronize()
+        assert ep.ep_get_status(status) == ep.EP_OK
+        assert np.array_equal(slot.cpu().numpy(), ref.slot)
+        assert np.array_equal(bits(recv), ref.recv_x)
+        assert np.array_equal(bits(y), ref.y)
+
+
 def test_dispatch_launch_counts(ep):
     """One launch wherever the tail does not apply: decode-size batches, a
     partial SM budget, launch overlap switched off."""
