@@ -102,8 +102,8 @@ struct DispatchArgs {
     // bytes equally fast: under the same load some finish an equal share of
     // the units 25-35 % later than others (by SM, the same pattern launch
     // after launch). So the ring launch takes all but the last tail_units,
-    // split evenly, and a second launch of many small CTAs (kTailWarps
-    // warps, one unit each) takes the rest; those CTAs need more shared
+    // split evenly, and a second launch of many small CTAs (2 or 4 warps,
+    // one unit each) takes the rest; those CTAs need more shared
     // memory than an SM has beside a ring CTA, so each starts only on an SM
     // whose ring CTA has finished, and the SMs that finish first take most
     // of the tail (the block scheduler serves as the work queue).
