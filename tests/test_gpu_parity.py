@@ -767,6 +767,42 @@ def test_combine_reads_the_rows_of_both_dispatch_launches(ep, graph):
         assert np.array_equal(bits(y), ref.y)
 
 
+def test_two_streams_dispatch_with_tails_at_once(ep):
+    """Two independent calls of ep_layout_dispatch + ep_combine, each large
+    enough for dispatch's tail launch, issued on two streams with nothing
+    ordering them: each tail's last CTA waits only for its own ring, and
+    both calls must match the oracle."""
+    T, H, E, K = 2100, 6144, 32, 8
+    dev = torch.device("cuda:0")
+    ep.ep_set_num_sms(0)
+    assert ep.ep_dispatch_launches(T, H, K) == 2
+    inps = [_custom(T, H, E, K, seed=90 + i, routing=r) for i, r in enumerate(("uniform", "zipf"))]
+    refs = [oracle_path(inp, T * K, 1.0) for inp in inps]
+    bufs = []
+    for inp in inps:
+        bufs.append(dict(idx=inp.topk_idx.to(dev), w=inp.topk_w.to(dev), x=inp.x.to(dev),
+                         counts=torch.empty(E, dtype=torch.int32, device=dev),
+                         offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                         slot=torch.empty((T, K), dtype=torch.int32, device=dev),
+                         recv=torch.zeros((T * K, H), dtype=torch.bfloat16, device=dev),
+                         y=torch.zeros((T, H), dtype=torch.bfloat16, device=dev),
+                         status=torch.zeros(1, dtype=torch.int32, device=dev)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for b, s in zip(bufs, streams):
+            with torch.cuda.stream(s):
+                ep.ep_layout_dispatch(b["idx"], E, b["x"], b["counts"], b["offsets"], b["slot"],
+                                      b["recv"], None, None, None, b["status"], s)
+                ep.ep_combine(b["recv"], b["slot"], b["w"], b["y"], b["status"], s)
+    torch.cuda.synchronize()
+    for b, ref in zip(bufs, refs):
+        assert ep.ep_get_status(b["status"]) == ep.EP_OK
+        assert np.array_equal(b["slot"].cpu().numpy(), ref.slot)
+        assert np.array_equal(bits(b["recv"]), ref.recv_x)
+        assert np.array_equal(bits(b["y"]), ref.y)
+
+
 def test_dispatch_launch_counts(ep):
     """One launch wherever the tail does not apply: decode-size batches, a
     partial SM budget, launch overlap switched off."""
