@@ -198,12 +198,13 @@ ep_status_t plan_dispatch(ep::DispatchArgs* a, const uint16_t* x, int64_t T, int
 
 // Default percentage of a full-budget dispatch's units that go to the tail
 // launch (DispatchArgs::tail_units; ep_set_dispatch_tail), for calls that
-// move at least kTailMinBytes of receive rows with K >= 2. Back to back, dispatch alone and the step with
-// combine after it: DeepSeek-V3 prefill (470 MB) 87.9 -> 76.8 and
-// 171.6 -> 162.9 us, skewed Zipf 80.7 -> 70.1 and 152.0 -> 146.6 us, T=16384
-// (1.9 GB) 352 -> 314 us for dispatch. A fifth to two fifths measured within
-// 1 us of each other. Smaller calls, mostly in L2, gain nothing; with K = 1
-// (as many bytes read as written) dispatch alone measured 2.5 us slower.
+// move at least kTailMinBytes of receive rows with K >= 2. Back to back,
+// dispatch alone and the step with combine after it: DeepSeek-V3 prefill
+// (470 MB) 87.9 -> 76.8 and 171.6 -> 162.9 us, skewed Zipf 80.7 -> 70.1 and
+// 152.0 -> 146.6 us, T=16384 (1.9 GB) 352 -> 314 us for dispatch. A fifth
+// to two fifths measured within 1 us of each other. Smaller calls, mostly
+// in L2, gain nothing; with K = 1 (as many bytes read as written) dispatch
+// alone measured 2.5 us slower.
 #ifndef EP_DISPATCH_TAIL_PERCENT
 #define EP_DISPATCH_TAIL_PERCENT 30
 #endif
