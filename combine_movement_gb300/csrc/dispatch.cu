@@ -56,6 +56,9 @@ namespace {
 #ifndef EP_DISPATCH_L2_PREFETCH
 #define EP_DISPATCH_L2_PREFETCH 1
 #endif
+#ifndef EP_DISPATCH_L2_TAIL
+#define EP_DISPATCH_L2_TAIL 1
+#endif
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr int kDispatchWarps = EP_DISPATCH_WARPS;
@@ -288,6 +291,22 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
                   a.x + t * static_cast<int64_t>(a.row_bytes) + off, bytes, bar, pol_load);
     };
 
+    // With a.tail_l2_prefetch, each warp also brings its share of the rows
+    // of the tail launch that follows (DispatchArgs::tail_units) into L2
+    // while the layout holds back its first store: the tail's CTAs start
+    // late, when HBM is busy with the ring's stores.
+    auto prefetch_tail_rows = [&](uint64_t policy) {
+        if (!EP_DISPATCH_L2_TAIL || !a.tail_l2_prefetch || a.tail_units <= 0) return;
+        const int64_t tb = a.unit_base + a.unit_count;
+        const int64_t q1 = tb + split_begin(a.tail_units, gw + 1, nw_total);
+        for (int64_t q = tb + split_begin(a.tail_units, gw, nw_total); q < q1; ++q) {
+            const int64_t qt = div_floor(q, a.n_chunks);
+            const uint32_t off = static_cast<uint32_t>(q - qt * a.n_chunks) * a.chunk_bytes;
+            bulk_prefetch_l2(a.x + qt * static_cast<int64_t>(a.row_bytes) + off,
+                             min(a.chunk_bytes, a.row_bytes - off), policy);
+        }
+    };
+
     // Loads issued before the ring starts: P, or the whole ring (NS) when
     // the kernel has to wait before its first store anyway (the fused
     // layout, or a layout kernel it overlaps) and no stage is being stored.
@@ -314,6 +333,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
                     ++pt;
                 }
             }
+            prefetch_tail_rows(pol_keep);
         }
 #endif
     };
@@ -578,6 +598,7 @@ cudaError_t launch_ring(const DispatchArgs& a, int num_sms, cudaStream_t stream)
     tail.tail = 1;
     tail.x_ready = 0;
     tail.l2_prefetch = 0;
+    tail.tail_l2_prefetch = 0;
     int dev = 0, per_sm = 0, reserved = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
     if ((err = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=

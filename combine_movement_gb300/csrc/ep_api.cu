@@ -209,6 +209,9 @@ ep_status_t plan_dispatch(ep::DispatchArgs* a, const uint16_t* x, int64_t T, int
 #define EP_DISPATCH_TAIL_PERCENT 30
 #endif
 constexpr int64_t kTailMinBytes = int64_t{192} << 20;
+// Largest share of x a ring launch prefetches for its tail (a quarter of
+// GB300's L2; DispatchArgs::tail_l2_prefetch).
+constexpr int64_t kTailPrefetchMaxBytes = int64_t{32} << 20;
 std::atomic<int> g_tail_percent{EP_DISPATCH_TAIL_PERCENT};
 
 // Tail units for this call (0: one persistent launch): only on the whole
@@ -385,6 +388,12 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
             a.x_ready = 1;
             a.l2_prefetch = n >= sm_count ? 1 : 0;
             a.tail_units = dispatch_tail_units(a, n, sm_count, s);
+            // the tail's x rows, when they fit a quarter of L2
+            a.tail_l2_prefetch =
+                (a.tail_units > 0 &&
+                 a.tail_units * static_cast<int64_t>(a.chunk_bytes) <= kTailPrefetchMaxBytes)
+                    ? 1
+                    : 0;
             return from_cuda(ep::launch_dispatch(a, n, smem_optin, s));
         }
     }

@@ -108,6 +108,12 @@ struct DispatchArgs {
     // whose ring CTA has finished, and the SMs that finish first take most
     // of the tail (the block scheduler serves as the work queue).
     int64_t tail_units;
+    // 1: the ring launch, while the layout kernel of ep_layout_dispatch
+    // holds back its first store, also brings the tail's rows of x into L2
+    // (when they take at most a quarter of L2; larger ones are evicted
+    // before the tail reads them). DeepSeek-V3 prefill step 162.4 ->
+    // 161.0 us; T=3072 125.6 -> 123.2 us.
+    int tail_l2_prefetch;
     // 1 in the tail launch: its CTAs start without waiting for the ring
     // launch (they only read what the ring launch read, which was complete
     // before the ring launch let them launch); its last CTA waits for the
