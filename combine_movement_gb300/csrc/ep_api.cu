@@ -127,6 +127,19 @@ bool use_combine_tma(int K, int num_sms) {
 // take the layout kernel and dispatch as two launches.
 constexpr int64_t kFusedMaxEntries = 4096;
 
+// Whether ep_layout_dispatch takes its two-launch form (the layout kernel,
+// then dispatch) for a table of T*K entries on `s`, with the layout's plan:
+// when the layout needs no workspace (one block, one 8-CTA cluster, or, for
+// a table just past that, one 16-CTA cluster where the GPU can hold it) and
+// either the table is too large for every CTA to histogram it cheaply, or
+// launches may overlap on this stream (then the second launch costs
+// nothing).
+bool layout_dispatch_two_launches(int64_t T, int K, int E, cudaStream_t s, ep::LayoutPlan* lp) {
+    *lp = ep::plan_layout(T * K, E);
+    if (lp->workspace_bytes != 0) (void)ep::plan_layout_wide_cluster(T * K, E, lp);
+    return lp->workspace_bytes == 0 && (T * K > kFusedMaxEntries || ep::launch_overlap_allowed(s));
+}
+
 // Host checks shared by ep_dispatch and ep_layout_dispatch.
 ep_status_t check_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const int32_t* slot,
                            const float* topk_w, int64_t num_recv, const uint16_t* recv_x,
@@ -289,6 +302,16 @@ int64_t ep_dispatch_chunk_bytes(int64_t T, int64_t H, int K) {
 
 int ep_dispatch_ring_stages(void) { return ep::dispatch_ring_stages(false, nullptr); }
 
+int ep_layout_dispatch_launches(int64_t T, int64_t H, int K, int E, void* stream) {
+    if (E < 1 || E > EP_MAX_EXPERTS) return -1;
+    const int d = ep_dispatch_launches(T, H, K, stream);
+    if (d <= 0) return d;
+    const ep::CallBytes call_bytes(T * K * 2 * H);
+    ep::LayoutPlan lp{};
+    const bool two = layout_dispatch_two_launches(T, K, E, static_cast<cudaStream_t>(stream), &lp);
+    return two ? 1 + d : 1;  // the two-launch form's layout is one launch
+}
+
 int ep_dispatch_launches(int64_t T, int64_t H, int K, void* stream) {
     if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || !row_fits(H) ||
         !pairs_fit(T, K))
@@ -375,9 +398,8 @@ ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64
     // the layout: its predecessor is that layout kernel, which does not
     // write x. Otherwise one launch does both.
     if (T > 0) {
-        const ep::LayoutPlan lp = ep::plan_layout(T * K, E);
-        if (lp.workspace_bytes == 0 &&
-            (T * K > kFusedMaxEntries || ep::launch_overlap_allowed(s))) {
+        ep::LayoutPlan lp{};
+        if (layout_dispatch_two_launches(T, K, E, s, &lp)) {
             cudaError_t e = ep::launch_layout(topk_idx, T * K, E, counts, offsets, slot, nullptr,
                                               lp, status, s);
             if (e != cudaSuccess) return EP_ERR_CUDA;

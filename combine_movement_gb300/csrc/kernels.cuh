@@ -56,6 +56,13 @@ struct LayoutPlan {
 
 LayoutPlan plan_layout(int64_t N, int E);
 
+// For tables that plan_layout gives a workspace but that fit one cluster of
+// up to 16 CTAs (a non-portable cluster size) where the GPU can hold it: a
+// plan for that cluster, with no workspace. For ep_layout_dispatch, which
+// has none; ep_get_dispatch_layout keeps the plan that depends on the sizes
+// alone (ep_layout_workspace_bytes). False where it does not apply.
+bool plan_layout_wide_cluster(int64_t N, int E, LayoutPlan* out);
+
 // `workspace` (16-byte aligned, plan.workspace_bytes) holds the barrier
 // words and the [tiles][E] counts.
 cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,

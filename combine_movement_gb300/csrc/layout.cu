@@ -299,6 +299,8 @@ __global__ void __launch_bounds__(kFinishThreads) layout_finish_kernel(
 //            may finish and exit on its own)
 //   phase 3  scan across experts, final slots; CTA 0 writes counts, offsets.
 constexpr int kClusterCtas = 8;  // portable cluster size
+// Non-portable cluster size for the wider variant (plan_layout_wide_cluster).
+constexpr int kWideClusterCtas = 16;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -321,6 +323,7 @@ __device__ __forceinline__ int32_t ld_cluster(uint32_t addr) {
     return v;
 }
 
+template <int CTAS>
 __global__ void __launch_bounds__(1024) layout_cluster_kernel(
     const int64_t* __restrict__ idx, int64_t N, int E, int rounds, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ slot, int32_t* status) {
@@ -379,13 +382,13 @@ __global__ void __launch_bounds__(1024) layout_cluster_kernel(
     int32_t* base = run + E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const uint32_t local = smem_u32(tile_tot + e);
-        int32_t c[kClusterCtas];
+        int32_t c[CTAS];
 #pragma unroll
-        for (int q = 0; q < kClusterCtas; ++q)
+        for (int q = 0; q < CTAS; ++q)
             c[q] = q < ntiles ? ld_cluster(cluster_map(local, static_cast<uint32_t>(q))) : 0;
         int32_t ts = 0, bs = 0;
 #pragma unroll
-        for (int q = 0; q < kClusterCtas; ++q) {
+        for (int q = 0; q < CTAS; ++q) {
             ts += c[q];
             bs += q < tile_id ? c[q] : 0;
         }
@@ -650,6 +653,49 @@ LayoutPlan plan_layout(int64_t N, int E) {
     return p;
 }
 
+bool plan_layout_wide_cluster(int64_t N, int E, LayoutPlan* out) {
+    LayoutPlan p = plan_layout(N, E);
+    const int64_t per_round = 32LL * p.warps;
+    if (p.workspace_bytes == 0 || N > per_round * kWideClusterCtas * kMaxRounds) return false;
+    p.rounds = static_cast<int>((N + per_round * kWideClusterCtas - 1) /
+                                (per_round * kWideClusterCtas));
+    p.tile = per_round * p.rounds;
+    p.num_tiles = static_cast<int>((N + p.tile - 1) / p.tile);
+    if (p.num_tiles <= kClusterCtas || p.num_tiles > kWideClusterCtas) return false;
+    p.smem = sizeof(int32_t) * static_cast<size_t>(E) * (p.warps + 1);
+    p.cluster = true;
+    p.coop = false;
+    p.counts_off = 0;
+    p.workspace_bytes = 0;
+    // only where this GPU can hold such a cluster at all
+    auto kern = layout_cluster_kernel<kWideClusterCtas>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(p.smem)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles));
+    cfg.blockDim = dim3(static_cast<unsigned>(p.warps * 32));
+    cfg.dynamicSmemBytes = p.smem;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(p.num_tiles);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    *out = p;
+    return true;
+}
+
 namespace {
 // Per-process epoch of the layout barriers' generation values: random, in
 // [2^63, 2^63 + 2^62).
@@ -686,10 +732,15 @@ cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,
                                 slot, status);
     }
     if (p.cluster) {
-        cudaError_t err = cudaFuncSetAttribute(layout_cluster_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const bool wide = p.num_tiles > kClusterCtas;
+        auto kern = wide ? layout_cluster_kernel<kWideClusterCtas> : layout_cluster_kernel<kClusterCtas>;
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(p.smem));
         if (err != cudaSuccess) return err;
+        if (wide &&
+            (err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
+                cudaSuccess)
+            return err;
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles));
         cfg.blockDim = dim3(static_cast<unsigned>(threads));
@@ -705,8 +756,7 @@ cudaError_t launch_layout(const int64_t* idx, int64_t N, int E, int32_t* counts,
         attr[1].val.programmaticStreamSerializationAllowed = launch_overlap_allowed(stream) ? 1 : 0;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, idx, N, E, p.rounds, counts, offsets,
-                                  slot, status);
+        return cudaLaunchKernelEx(&cfg, kern, idx, N, E, p.rounds, counts, offsets, slot, status);
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint64_t* sync = reinterpret_cast<uint64_t*>(ws);

@@ -88,6 +88,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_dispatch_chunk_bytes.restype = i64
     lib.ep_dispatch_launches.argtypes = [i64, i64, i32, p]
     lib.ep_dispatch_launches.restype = i32
+    lib.ep_layout_dispatch_launches.argtypes = [i64, i64, i32, i32, p]
+    lib.ep_layout_dispatch_launches.restype = i32
     lib.ep_get_dispatch_layout.argtypes = [p, i64, i32, i32, p, p, p, p, sz, p, p]
     lib.ep_get_dispatch_layout.restype = i32
     lib.ep_dispatch.argtypes = [p, i64, i64, i32, p, p, i64, p, p, p, p, p]
@@ -199,6 +201,10 @@ def ep_dispatch_ring_stages() -> int:
 
 def ep_dispatch_launches(T: int, H: int, K: int, stream=None) -> int:
     return int(lib.ep_dispatch_launches(T, H, K, _stream(stream)))
+
+
+def ep_layout_dispatch_launches(T: int, H: int, K: int, E: int, stream=None) -> int:
+    return int(lib.ep_layout_dispatch_launches(T, H, K, E, _stream(stream)))
 
 
 def ep_status_string(code: int) -> str:

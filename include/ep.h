@@ -177,6 +177,12 @@ EP_API int ep_dispatch_ring_stages(void);
  * cannot be queried. */
 EP_API int ep_dispatch_launches(int64_t T, int64_t H, int K, void* stream);
 
+/* Kernel launches one ep_layout_dispatch call makes for these sizes on
+ * `stream` at the current SM budget and launch-overlap mode: 1 in its
+ * one-launch form, else 1 for the layout plus ep_dispatch_launches. -1 for
+ * invalid sizes or when the device cannot be queried. */
+EP_API int ep_layout_dispatch_launches(int64_t T, int64_t H, int K, int E, void* stream);
+
 /* Layout (per-expert histogram, exclusive prefix sums and per-(token,k)
  * destination slot).
  *   topk_idx   int64 [T][K]   routing table (DeepEP's topk_idx)
@@ -225,15 +231,19 @@ EP_API ep_status_t ep_dispatch(const uint16_t* x, int64_t T, int64_t H, int K,
  *    which every CTA reads the whole routing table and lays out its own
  *    tokens (on GB300, T=128 top-8 on 24 SMs: a layout + dispatch + combine
  *    step takes 29.4 us with it, 33.4 us with the separate calls).
- *  - Otherwise, when the layout needs no workspace (at most 65,536 entries
- *    at E <= 256): the layout kernel and the dispatch kernel, with
- *    dispatch's first row loads (its whole ring; at the full SM budget also
- *    the next rows, into L2) issued while the layout runs (safe because
- *    this call launched that layout kernel itself, which never writes x):
- *    on GB300 the DeepSeek-V3 prefill step (T=4096 top-8, H=7168) takes
- *    0.162 ms with it and 0.165 ms with the separate calls.
+ *  - Otherwise, when the layout needs no workspace (one block or one
+ *    thread-block cluster: at most 65,536 entries at E <= 256, or 131,072
+ *    with a 16-CTA cluster where the GPU can hold one): the layout kernel
+ *    and the dispatch kernel, with dispatch's first row loads (its whole
+ *    ring; at the full SM budget also the next rows, into L2) issued while
+ *    the layout runs (safe because this call launched that layout kernel
+ *    itself, which never writes x): on GB300 the DeepSeek-V3 prefill step
+ *    (T=4096 top-8, H=7168) takes 0.161-0.163 ms with it and 0.165 ms with
+ *    the separate calls; T=16384 (131,072 entries, the 16-CTA cluster)
+ *    0.635 vs 0.645 ms.
  *  - Larger tables fall back to the one-launch form, whose cost grows with
- *    T*K per CTA; call the two functions separately for those.
+ *    T*K per CTA; call the two functions separately for those
+ *    (ep_layout_dispatch_launches tells the forms apart).
  * Arguments as in those two calls; T == 0 still writes zero counts and
  * offsets. */
 EP_API ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x, int64_t T,

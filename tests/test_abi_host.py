@@ -112,6 +112,9 @@ def test_dispatch_launches_rejects_invalid_sizes(ep):
     assert ep.lib.ep_dispatch_launches(4096, 7168, 33, None) == -1  # K above the limit
     assert ep.lib.ep_dispatch_launches(-1, 7168, 8, None) == -1
     assert ep.lib.ep_dispatch_launches(0, 7168, 8, None) == 0       # nothing to launch
+    assert ep.lib.ep_layout_dispatch_launches(4096, 7168, 8, 0, None) == -1      # E < 1
+    assert ep.lib.ep_layout_dispatch_launches(4096, 7168, 8, 5000, None) == -1   # E too large
+    assert ep.lib.ep_layout_dispatch_launches(4096, 7166, 8, 256, None) == -1    # H % 8 != 0
 
 
 def test_dispatch_chunk_bytes_rejects_invalid_sizes(ep):

@@ -803,6 +803,32 @@ def test_two_streams_dispatch_with_tails_at_once(ep):
         assert np.array_equal(bits(b["y"]), ref.y)
 
 
+@pytest.mark.parametrize("T,H,E,K,mask,budget", [
+    (16384, 64, 128, 8, 0.0, 0),    # 131,072 entries: 16 tiles of 8 rounds, the most it takes
+    (9000, 32, 256, 8, 0.1, 0),     # 72,000 entries: 15 tiles of 5 rounds, masked
+    (8200, 8, 33, 8, 0.0, 24),      # 65,600 entries, just past one 8-CTA cluster; partial budget
+    (4100, 16, 64, 16, 0.05, 0),    # K = 16
+])
+def test_layout_dispatch_wide_cluster(ep, T, H, E, K, mask, budget):
+    """Tables just past what one 8-CTA cluster lays out (65,536 entries at
+    E <= 256) would need a workspace; ep_layout_dispatch, which has none,
+    lays them out with one 16-CTA cluster (a non-portable cluster size) and
+    keeps its two-launch form. Slots, rows and combine against the oracle,
+    and the same results through the three separate calls (whose layout
+    keeps its workspace)."""
+    inp = _custom(T, H, E, K, seed=T + E, mask=mask)
+    R_valid = int((inp.topk_idx >= 0).sum())
+    ref = oracle_path(inp, R_valid, 1.0)
+    assert ep.ep_layout_workspace_bytes(T, K, E) > 0
+    ep.ep_set_num_sms(budget)
+    try:
+        assert ep.ep_layout_dispatch_launches(T, H, K, E) >= 2   # the layout kernel, then dispatch
+    finally:
+        ep.ep_set_num_sms(0)
+    for fused in (True, False):
+        assert_parity(gpu_path(ep, inp, R_valid, ref.expert_out, num_sms=budget, fused=fused), ref)
+
+
 def test_dispatch_launch_counts(ep):
     """One launch wherever the tail does not apply: decode-size batches, a
     partial SM budget, launch overlap switched off."""
@@ -811,6 +837,8 @@ def test_dispatch_launch_counts(ep):
     assert ep.ep_dispatch_launches(128, 7168, 8) == 1
     assert ep.ep_dispatch_launches(1024, 7168, 8) == 1     # 117 MB of rows
     assert ep.ep_dispatch_launches(16384, 7168, 1) == 1    # K = 1
+    assert ep.ep_layout_dispatch_launches(4096, 7168, 8, 256) == 3   # layout, ring, tail
+    assert ep.ep_layout_dispatch_launches(128, 7168, 8, 256) == 2    # layout, dispatch
     mode = ep.ep_get_launch_overlap()
     try:
         ep.ep_set_launch_overlap(2)
@@ -820,6 +848,8 @@ def test_dispatch_launch_counts(ep):
     try:
         ep.ep_set_num_sms(24)
         assert ep.ep_dispatch_launches(4096, 7168, 8) == 1
+        assert ep.ep_layout_dispatch_launches(128, 7168, 8, 256) == 1    # one launch
+        assert ep.ep_layout_dispatch_launches(4096, 7168, 8, 256) == 2   # more than 4096 entries
     finally:
         ep.ep_set_num_sms(0)
 
