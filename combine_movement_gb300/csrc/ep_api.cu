@@ -127,6 +127,10 @@ bool use_combine_tma(int K, int num_sms) {
 // take the layout kernel and dispatch as two launches.
 constexpr int64_t kFusedMaxEntries = 4096;
 
+#ifndef EP_LAYOUT_WIDE_CLUSTER
+#define EP_LAYOUT_WIDE_CLUSTER 1
+#endif
+
 // Whether ep_layout_dispatch takes its two-launch form (the layout kernel,
 // then dispatch) for a table of T*K entries on `s`, with the layout's plan:
 // when the layout needs no workspace (one block, one 8-CTA cluster, or, for
@@ -342,10 +346,15 @@ ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, in
     if (!aligned(topk_idx, 8) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(slot, 4) ||
         !aligned(status, 4))
         return EP_ERR_INVALID;
-    const ep::LayoutPlan plan = ep::plan_layout(T * K, E);
+    ep::LayoutPlan plan = ep::plan_layout(T * K, E);
     if (plan.workspace_bytes > 0) {
         if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return EP_ERR_WORKSPACE;
         if (!aligned(workspace, 16)) return EP_ERR_INVALID;
+#if EP_LAYOUT_WIDE_CLUSTER
+        // the workspace is asked for by size alone; a table that one 16-CTA
+        // cluster can lay out leaves it unused where the GPU holds one
+        (void)ep::plan_layout_wide_cluster(T * K, E, &plan);
+#endif
     }
     return from_cuda(ep::launch_layout(topk_idx, T * K, E, counts, offsets, slot, workspace, plan,
                                        status, static_cast<cudaStream_t>(stream)));

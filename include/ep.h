@@ -195,7 +195,10 @@ EP_API int ep_layout_dispatch_launches(int64_t T, int64_t H, int K, int E, void*
  *              barrier; any initial content is valid, so it never needs
  *              clearing, and within a process the barrier's targets never
  *              repeat. Calls that share a workspace must not overlap on the
- *              GPU.
+ *              GPU. Tables that one 16-CTA thread-block cluster can lay out
+ *              (up to 131,072 entries at E <= 256) leave it unused where the
+ *              GPU can hold such a cluster; its size still depends on the
+ *              sizes alone.
  *   status     int32 device word, nullable (device errors: BAD_EXPERT)
  * T == 0 is valid (counts and offsets are zeroed). */
 EP_API ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t T, int K, int E,

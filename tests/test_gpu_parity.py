@@ -190,7 +190,8 @@ def _custom(T, H, E, K, seed=7, mask=0.0, routing="uniform"):
     (300, 7176, 64, 8, 0.0),    # H not a multiple of the chunk or 512-byte block
     (500, 1024, 128, 6, 0.3),   # masked entries (-1)
     (64, 256, 4096, 8, 0.0),    # maximum expert count, mostly empty experts
-    (2048, 256, 4096, 8, 0.0),  # maximum expert count, multi-tile layout
+    (2048, 256, 4096, 8, 0.0),  # maximum expert count, one 16-CTA cluster (else cooperative)
+    (2100, 256, 4096, 8, 0.0),  # maximum expert count, just past it: cooperative layout
     (40, 64, 40, 32, 0.0),      # maximum K (generic combine path)
     (100, 128, 16, 12, 0.1),    # K above the specialised range, masked
     (9000, 64, 256, 1, 0.0),    # K = 1, multi-tile layout
@@ -572,7 +573,8 @@ def test_heterogeneous_batches_back_to_back(ep, budget, mode):
 @pytest.mark.parametrize("T,H,E,K", [
     (128, 7168, 256, 8),   # decode: one-block layout
     (2048, 2048, 64, 8),   # one thread-block cluster layout
-    (16384, 64, 128, 8),   # cooperative layout (grid barrier, generation word)
+    (16384, 64, 128, 8),   # one 16-CTA cluster (where the GPU holds one; else cooperative)
+    (20000, 64, 128, 8),   # cooperative layout (grid barrier, generation word)
 ])
 def test_cuda_graph_capture_and_replay(ep, T, H, E, K):
     """The three calls captured once into a CUDA graph (with the expert
