@@ -67,3 +67,38 @@ def test_cluster_layout_matches_oracle(ep, E, label, n):
     assert np.array_equal(counts.cpu().numpy(), c_ref), "counts"
     assert np.array_equal(offsets.cpu().numpy(), o_ref), "offsets"
     assert np.array_equal(slot.cpu().numpy(), s_ref), "slot"
+
+
+def _wide_cases():
+    out = []
+    for E in (2, 7, 33, 257, 1000, 3001, 4096):
+        r = _round_entries(E)
+        # 13 CTAs of 5 rounds, 15 of 7, 16 of 8
+        for label, n in (("13-ctas", 64 * r + 1), ("15-ctas", 104 * r - 5), ("largest", 128 * r)):
+            out.append((E, label, n))
+    return out
+
+
+@pytest.mark.parametrize("E,label,n", _wide_cases())
+def test_wide_cluster_layout_matches_oracle(ep, E, label, n):
+    """Tables of 65 to 128 rounds: ep_get_dispatch_layout asks for a
+    workspace (by size alone) but lays them out with one cluster of 13 to
+    16 CTAs (a non-portable cluster size) where the GPU can hold one, else
+    with the cooperative launch; either way exactly the oracle's layout."""
+    K = min(8, E)
+    T = (n + K - 1) // K
+    if T * K > 128 * _round_entries(E):
+        T = 128 * _round_entries(E) // K
+    assert ep.ep_layout_workspace_bytes(T, K, E) > 0
+    mask = 0.1 if E in (33, 3001) else 0.0
+    wl = W.Workload(f"wide-E{E}-{label}", T=T, H=8, E=E, K=K, seed=E + n, mask_frac=mask)
+    idx_cpu = W.make_inputs(wl).topk_idx
+    c_ref, o_ref, s_ref, st = oracle.Oracle().layout(idx_cpu.numpy(), E)
+    assert st == 0
+    dev = torch.device("cuda:0")
+    counts, offsets, slot = ep.get_dispatch_layout(idx_cpu.to(dev), E)
+    torch.cuda.synchronize()
+    assert np.array_equal(counts.cpu().numpy(), c_ref), "counts"
+    assert np.array_equal(offsets.cpu().numpy(), o_ref), "offsets"
+    assert np.array_equal(slot.cpu().numpy(), s_ref), "slot"
+
