@@ -127,8 +127,11 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(const int64_t* topk_idx, i
     if (!aligned(topk_idx, 8) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(slot, 4) ||
         !aligned(status, 4))
         return EP_ERR_INVALID;
-    const ep::LayoutPlan plan = ep::plan_layout(T * K, E);
+    ep::LayoutPlan plan = ep::plan_layout(T * K, E);
     if (plan.workspace_bytes > kLayoutScratchBytes) return EP_ERR_UNSUPPORTED;
+    // a table that one 16-CTA cluster can lay out needs no scratch at all
+    // where the GPU holds one (and then shares nothing with other calls)
+    if (plan.workspace_bytes > 0) (void)ep::plan_layout_wide_cluster(T * K, E, &plan);
     void* scratch = nullptr;
     if (plan.workspace_bytes > 0) {
         const ep_status_t st = scratch_address(&scratch);

@@ -285,7 +285,9 @@ EP_API ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv,
  *    call on that device (again outside any capture) looks the address up
  *    anew, and the array's contents start over.
  *  - Sharing: all calls share the array. Calls that overlap on the GPU (other
- *    streams or host threads) race on it; order them. Nothing in it needs to
+ *    streams or host threads) race on it; order them. Tables that one
+ *    16-CTA thread-block cluster lays out (up to 131,072 entries at
+ *    E <= 256, where the GPU holds such a cluster) do not use it. Nothing in it needs to
  *    start at zero: each call rewrites the counts it reads, and the one word
  *    it carries between calls is valid from any starting value. */
 #define EP_NOALLOC_SCRATCH_BYTES (1u << 20)

@@ -83,20 +83,23 @@ def test_noalloc_matches_oracle_on_consecutive_calls(ep):
         pytest.skip("no CUDA device")
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    # Tables large enough to need scratch (smaller ones are laid out by one
-    # thread-block cluster, with none). The two launch shapes that use it,
-    # in a sequence where each call finds the previous one's contents:
+    # Tables large enough to need scratch by size (smaller ones are laid out
+    # by one thread-block cluster, with none; up to 131,072 entries at
+    # E <= 256 a 16-CTA cluster takes them without scratch where the GPU
+    # holds one: 16384 x 8 at E = 128 here). The two launch shapes that use
+    # it, in a sequence where each call finds the previous one's contents:
     #  - up to 128 tiles: one cooperative launch whose grid barrier keeps
-    #    its words in the scratch (16384 x 8 at E = 128 and 512: 128 tiles);
+    #    its words in the scratch (20000 x 8 at E = 128 and 512: 20 tiles);
     #  - more tiles: tile + finish launches (140000 x 8 at E = 128: 137
     #    tiles, 70 KB of per-tile counts);
     #  - then a cooperative call with another tile count (9000 x 8 at
     #    E = 1024: 71 tiles), whose flag words still hold earlier targets.
     big = W.Workload("noalloc-137-tiles", T=140000, H=8, E=128, K=8, seed=12)
     small_coop = W.Workload("noalloc-coop-71-tiles", T=9000, H=8, E=1024, K=8, seed=13)
-    cases = [W.sweep(16384, 64),
-             W.Workload("noalloc-e512", T=16384, H=64, E=512, K=8, seed=11),
-             big, small_coop, big, W.sweep(16384, 64)]
+    coop20 = W.Workload("noalloc-coop-20-tiles", T=20000, H=8, E=128, K=8, seed=14)
+    cases = [coop20, W.sweep(16384, 64),
+             W.Workload("noalloc-e512", T=20000, H=64, E=512, K=8, seed=11),
+             big, small_coop, big, coop20]
     for wl in cases:
         assert 0 < ep.ep_layout_workspace_bytes(wl.T, wl.K, wl.E) <= ep.EP_NOALLOC_SCRATCH_BYTES
     assert ep.ep_layout_launches(big.T, big.K, big.E) == 2
