@@ -190,8 +190,10 @@ class Step:
         self.b.idx.copy_(inp.topk_idx)
         self.b.w.copy_(inp.topk_w)
         self.layout_launches = ep.ep_layout_launches(self.T, self.K, self.E)
-        # 2 where dispatch adds a tail launch (the whole GPU, prefill sizes)
+        # 2 where dispatch or combine adds a tail launch (the whole GPU,
+        # prefill sizes)
         self.dispatch_launches = ep.ep_dispatch_launches(self.T, self.H, self.K)
+        self.combine_launches = ep.ep_combine_launches(self.T, self.H, self.K)
         # x larger than 8 MB is rotated over four device copies, so that no
         # dispatch finds the previous call's x in L2 (the rotated copies
         # together exceed it); decode-size x stays warm, as in a decode loop
@@ -237,7 +239,7 @@ class Step:
 
     @property
     def launches_per_step(self) -> int:
-        return self.layout_launches + self.dispatch_launches + 1
+        return self.layout_launches + self.dispatch_launches + self.combine_launches
 
 
 def barrier(dist_on: bool):
@@ -334,17 +336,17 @@ def time_steps(step: Step, steps: int, warmup: int, dist_on: bool, stream: torch
             "clocks": sampler.summary() if sampler else None}
 
 
-def dispatch_b2b_us(step: Step, stream, n: int) -> float:
-    """Average duration of n dispatch calls back to back on `stream` (CUDA
-    events around the loop only)."""
+def calls_b2b_us(fn, stream, n: int) -> float:
+    """Average duration of n calls of fn(stream) back to back on `stream`
+    (CUDA events around the loop only)."""
     with torch.cuda.stream(stream):
         for _ in range(3):
-            step.dispatch(step.b, stream)
+            fn(stream)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(n):
-            step.dispatch(step.b, stream)
+            fn(stream)
         e1.record(stream)
         torch.cuda.synchronize()
     return e0.elapsed_time(e1) / n * 1e3
@@ -1364,6 +1366,8 @@ def main():
                     help="percentage of a full-GPU dispatch's units its tail launch takes "
                          "(ep_set_dispatch_tail; 0: one persistent launch; default: the "
                          "library's)")
+    ap.add_argument("--combine-tail", type=int, default=-1,
+                    help="the same for combine (ep_set_combine_tail)")
     ap.add_argument("--ncu-budgets", action="store_true",
                     help="for profiling: one layout+dispatch+combine step at each SM budget "
                          "(16, 24, 48, all), after one warm-up step")
@@ -1395,6 +1399,8 @@ def main():
     from combine_movement_gb300 import ep
     if args.dispatch_tail >= 0 and ep.ep_set_dispatch_tail(args.dispatch_tail) < 0:
         raise SystemExit("--dispatch-tail must be in [0, 90]")
+    if args.combine_tail >= 0 and ep.ep_set_combine_tail(args.combine_tail) < 0:
+        raise SystemExit("--combine-tail must be in [0, 90]")
 
     if args.overlap:
         if rank == 0:
@@ -1474,12 +1480,17 @@ def main():
     ep.ep_set_num_sms(args.budget_sms)
     fused_budget = time_fused_steps(step, args.steps, args.warmup, dist_on, stream)
     ep.ep_set_num_sms(0)
-    # dispatch back to back without its tail launch (one persistent launch),
-    # beside the same figure with it (main_run's b2b)
+    # dispatch and combine back to back without their tail launches (one
+    # persistent launch each), beside the same figures with them (main_run)
+    n_b2b = max(50, min(args.steps, 500))
     tail_pct = ep.ep_get_dispatch_tail()
     ep.ep_set_dispatch_tail(0)
-    no_tail_b2b_us = dispatch_b2b_us(step, stream, max(50, min(args.steps, 500)))
+    no_tail_b2b_us = calls_b2b_us(lambda s: step.dispatch(step.b, s), stream, n_b2b)
     ep.ep_set_dispatch_tail(tail_pct)
+    ctail_pct = ep.ep_get_combine_tail()
+    ep.ep_set_combine_tail(0)
+    no_ctail_b2b_us = calls_b2b_us(lambda s: step.combine(step.b, s), stream, n_b2b)
+    ep.ep_set_combine_tail(ctail_pct)
     e2e = time_e2e(step, inp, max(3, min(args.steps, 200)), 3)
     ceil = per_sm_ceilings(dev, (16, args.budget_sms, 0)) if rank == 0 else {}
     decode = decode_latency(ep, dev, (16, args.budget_sms, 0), ceil) if rank == 0 else None
@@ -1581,13 +1592,20 @@ def main():
                 "nominal_peak_gbs": NOMINAL_HBM_GBS,
                 "algorithmic_bytes_per_step": ab,
             },
-            # dispatch's split into a persistent launch and a tail launch
-            # (ep_dispatch_launches): its calls back to back with and without
+            # dispatch's and combine's split into a persistent launch and a
+            # tail launch (ep_dispatch_launches, ep_combine_launches): their
+            # calls back to back with and without
             "dispatch_tail": {
                 "percent": tail_pct,
                 "launches_per_call": step.dispatch_launches,
                 "b2b_us": s_all["b2b_us"]["dispatch"],
                 "b2b_us_one_launch": no_tail_b2b_us,
+            },
+            "combine_tail": {
+                "percent": ctail_pct,
+                "launches_per_call": step.combine_launches,
+                "b2b_us": s_all["b2b_us"]["combine"],
+                "b2b_us_one_launch": no_ctail_b2b_us,
             },
             "roofline": {
                 "bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,

@@ -73,6 +73,13 @@ constexpr int kGenericWideSms = 96;
 constexpr int kSmallThreads = 384;
 constexpr int kSmallUnroll = 2;
 
+#ifndef EP_COMBINE_TAIL_WARPS
+#define EP_COMBINE_TAIL_WARPS 4
+#endif
+#ifndef EP_COMBINE_TAIL_UNITS
+#define EP_COMBINE_TAIL_UNITS 2
+#endif
+
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr uint32_t kColBytes = 512;  // row bytes one warp covers per column block
 constexpr int kGenericBatch = 8;     // k entries per batch of loads in the generic path
@@ -83,17 +90,18 @@ constexpr int kGenericBatch = 8;     // k entries per batch of loads in the gene
 // UN * K independent 16-byte loads in flight.
 template <int KT, int kThreads, int kUnroll, bool kFast, bool kSlotRows>
 __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const CombineArgs a) {
-    griddep_wait();
+    if (!a.tail || blockIdx.x == gridDim.x - 1) griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     constexpr uint32_t kUnitBytes = kColBytes * kUnroll;
     const int64_t n_cb = (a.row_bytes + kUnitBytes - 1) / kUnitBytes;
-    const int64_t units = a.T * n_cb;
+    // this launch's units, split evenly over its warps
+    const int64_t units = a.unit_count;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t nw_total = static_cast<int64_t>(gridDim.x) * nwarps;
-    const int64_t u0 = split_begin(units, gw, nw_total);
-    const int64_t u1 = split_begin(units, gw + 1, nw_total);
+    const int64_t u0 = a.unit_base + split_begin(units, gw, nw_total);
+    const int64_t u1 = a.unit_base + split_begin(units, gw + 1, nw_total);
     const int K = KT > 0 ? KT : a.K;
     constexpr int KR = KT > 0 ? KT : 1;
 
@@ -236,14 +244,30 @@ cudaError_t launch_shape(const CombineArgs& a, int num_sms, cudaStream_t stream)
     constexpr uint32_t kUnitBytes = kColBytes * kUnroll;
     const int64_t units = a.T * ((a.row_bytes + kUnitBytes - 1) / kUnitBytes);
     const int64_t warps_per_cta = kThreads / 32;
-    const int64_t ctas_needed = (units + warps_per_cta - 1) / warps_per_cta;
+    // a.tail_percent of the units to a tail launch (as dispatch's: small
+    // CTAs that start on SMs as the persistent CTAs leave them; a combine
+    // CTA holds the whole register file, so nothing shares its SM)
+    const int64_t tail = units * a.tail_percent / 100;
+    CombineArgs main = a;
+    main.unit_base = 0;
+    main.unit_count = units - tail;
+    const int64_t ctas_needed = (main.unit_count + warps_per_cta - 1) / warps_per_cta;
     const int grid = static_cast<int>(ctas_needed < num_sms ? ctas_needed : num_sms);
     if (grid <= 0) return cudaSuccess;
     auto kern = combine_kernel<KT, kThreads, kUnroll, kFast, kSlotRows>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kExclusiveSmem));
     if (err != cudaSuccess) return err;
-    return launch_dependent(kern, grid, kThreads, kExclusiveSmem, stream, a);
+    err = launch_dependent(kern, grid, kThreads, kExclusiveSmem, stream, main);
+    if (err != cudaSuccess || tail <= 0) return err;
+    CombineArgs t = a;
+    t.unit_base = main.unit_count;
+    t.unit_count = tail;
+    t.tail = 1;
+    constexpr int kTailThreads = EP_COMBINE_TAIL_WARPS * 32;
+    const int64_t per_cta = static_cast<int64_t>(EP_COMBINE_TAIL_WARPS) * EP_COMBINE_TAIL_UNITS;
+    const int tail_grid = static_cast<int>((tail + per_cta - 1) / per_cta);
+    return launch_dependent(kern, tail_grid, kTailThreads, 0, stream, t);
 }
 
 // CTAs a shape needs for one unit per warp.

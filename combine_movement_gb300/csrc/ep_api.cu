@@ -226,6 +226,25 @@ ep_status_t plan_dispatch(ep::DispatchArgs* a, const uint16_t* x, int64_t T, int
 #define EP_DISPATCH_TAIL_PERCENT 30
 #endif
 constexpr int64_t kTailMinBytes = int64_t{192} << 20;
+// Default percentage of a combine's units that go to a tail launch, under
+// the same conditions as dispatch's (ep_set_combine_tail). Its SMs spread
+// less than dispatch's, but a tail still helps: back to back, DeepSeek-V3
+// prefill combine 78.9 -> 76.3 us, T=16384 316.5 -> 304.6 us; the steps
+// with dispatch 162.1 -> 161.8, 635.5 -> 628.5 and skewed Zipf 147.4 ->
+// 145.9 us (10 % and 20 % measured between none and this).
+#ifndef EP_COMBINE_TAIL_PERCENT
+#define EP_COMBINE_TAIL_PERCENT 30
+#endif
+std::atomic<int> g_combine_tail_percent{EP_COMBINE_TAIL_PERCENT};
+
+// Tail share for this combine call (0: one persistent launch): as
+// dispatch_tail_units, on the whole GPU with launches overlapping, for
+// calls of at least kTailMinBytes of rows with K >= 2.
+int combine_tail_percent(int64_t T, int64_t H, int K, int n, int sm_count, cudaStream_t s) {
+    const int percent = g_combine_tail_percent.load(std::memory_order_relaxed);
+    if (percent <= 0 || K < 2 || n < sm_count || !ep::launch_overlap_allowed(s)) return 0;
+    return T * K * 2 * H >= kTailMinBytes ? percent : 0;
+}
 // Largest share of x a ring launch prefetches for its tail (a quarter of
 // GB300's L2; DispatchArgs::tail_l2_prefetch).
 constexpr int64_t kTailPrefetchMaxBytes = int64_t{32} << 20;
@@ -270,6 +289,28 @@ int ep_set_dispatch_tail(int percent) {
 }
 
 int ep_get_dispatch_tail(void) { return g_tail_percent.load(std::memory_order_relaxed); }
+
+int ep_set_combine_tail(int percent) {
+    if (percent < 0 || percent > 90) return -1;
+    g_combine_tail_percent.store(percent, std::memory_order_relaxed);
+    return percent;
+}
+
+int ep_get_combine_tail(void) { return g_combine_tail_percent.load(std::memory_order_relaxed); }
+
+int ep_combine_launches(int64_t T, int64_t H, int K, void* stream) {
+    if (T < 0 || H <= 0 || H % 8 != 0 || K < 1 || K > EP_MAX_TOPK || !row_fits(H) ||
+        !pairs_fit(T, K))
+        return -1;
+    if (T == 0) return 0;
+    const ep::CallBytes call_bytes(T * K * 2 * H);
+    int sm_count = 0, smem_optin = 0;
+    if (!device_limits(&sm_count, &smem_optin)) return -1;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int n = sms_for_stream(sm_count, s);
+    if (use_combine_tma(K, n)) return 1;
+    return combine_tail_percent(T, H, K, n, sm_count, s) > 0 ? 2 : 1;
+}
 
 int ep_num_sms_in_effect(void) {
     int c = 0, s = 0;
@@ -471,6 +512,7 @@ ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv, const int32
     a.y = reinterpret_cast<uint8_t*>(y);
     a.status = status;
     const int n = sms_for_stream(sm_count, static_cast<cudaStream_t>(stream));
+    a.tail_percent = combine_tail_percent(T, H, K, n, sm_count, static_cast<cudaStream_t>(stream));
     if (use_combine_tma(K, n))
         return from_cuda(ep::launch_combine_tma(a, n, smem_optin, static_cast<cudaStream_t>(stream)));
     return from_cuda(ep::launch_combine(a, n, static_cast<cudaStream_t>(stream)));

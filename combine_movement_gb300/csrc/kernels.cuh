@@ -176,6 +176,16 @@ struct CombineArgs {
     int K;
     uint8_t* y;
     int32_t* status;
+    // Percentage of the units a tail launch takes (0: one persistent
+    // launch); set by the host where dispatch's tail applies, see
+    // launch_shape in combine.cu.
+    int tail_percent;
+    // Set by launch_shape per launch: units [unit_base, unit_base +
+    // unit_count) of the shape's T * column-block units, and 1 in the tail
+    // launch (its CTAs skip the wait for the persistent launch but the last).
+    int64_t unit_base;
+    int64_t unit_count;
+    int tail;
 };
 
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t stream);

@@ -76,6 +76,12 @@ def _load() -> ctypes.CDLL:
     lib.ep_set_dispatch_tail.restype = i32
     lib.ep_get_dispatch_tail.argtypes = []
     lib.ep_get_dispatch_tail.restype = i32
+    lib.ep_set_combine_tail.argtypes = [i32]
+    lib.ep_set_combine_tail.restype = i32
+    lib.ep_get_combine_tail.argtypes = []
+    lib.ep_get_combine_tail.restype = i32
+    lib.ep_combine_launches.argtypes = [i64, i64, i32, p]
+    lib.ep_combine_launches.restype = i32
     lib.ep_num_sms_in_effect.argtypes = []
     lib.ep_num_sms_in_effect.restype = i32
     lib.ep_layout_workspace_bytes.argtypes = [i64, i32, i32]
@@ -177,6 +183,18 @@ def ep_set_dispatch_tail(percent: int) -> int:
 
 def ep_get_dispatch_tail() -> int:
     return lib.ep_get_dispatch_tail()
+
+
+def ep_set_combine_tail(percent: int) -> int:
+    return lib.ep_set_combine_tail(int(percent))
+
+
+def ep_get_combine_tail() -> int:
+    return lib.ep_get_combine_tail()
+
+
+def ep_combine_launches(T: int, H: int, K: int, stream=None) -> int:
+    return int(lib.ep_combine_launches(T, H, K, _stream(stream)))
 
 
 def ep_num_sms_in_effect() -> int:

@@ -133,6 +133,13 @@ EP_API int ep_get_launch_overlap(void);
 EP_API int ep_set_dispatch_tail(int percent);
 EP_API int ep_get_dispatch_tail(void);
 
+/* The same for combine (0 to 90, default 30): under the same conditions as
+ * dispatch's tail (ep_combine_launches), combine hands that share of its
+ * (token, column block) units to a second launch of small CTAs. Returns the
+ * stored value, or -1 (and changes nothing) outside that range. */
+EP_API int ep_set_combine_tail(int percent);
+EP_API int ep_get_combine_tail(void);
+
 /* The number of SMs dispatch/combine will use on the current device: the
  * budget clamped to [1, SM count]. Returns -1 if the device can't be queried. */
 EP_API int ep_num_sms_in_effect(void);
@@ -182,6 +189,13 @@ EP_API int ep_dispatch_launches(int64_t T, int64_t H, int K, void* stream);
  * one-launch form, else 1 for the layout plus ep_dispatch_launches. -1 for
  * invalid sizes or when the device cannot be queried. */
 EP_API int ep_layout_dispatch_launches(int64_t T, int64_t H, int K, int E, void* stream);
+
+/* Kernel launches one ep_combine call makes for these sizes on `stream` at
+ * the current SM budget and launch-overlap mode: 2 where it hands part of
+ * its units to a tail launch (the whole GPU, launches overlapping, at least
+ * 192 MB of rows, K >= 2, a combine tail share above 0), else 1. -1 for
+ * invalid sizes or when the device cannot be queried. */
+EP_API int ep_combine_launches(int64_t T, int64_t H, int K, void* stream);
 
 /* Layout (per-expert histogram, exclusive prefix sums and per-(token,k)
  * destination slot).
@@ -261,7 +275,10 @@ EP_API ep_status_t ep_layout_dispatch(const int64_t* topk_idx, const uint16_t* x
  *   slot       int32 [T][K]
  *   topk_w     fp32 [T][K]         routing weights in token order
  *   y          bf16 [T][H] out
- * A token whose K entries are all skipped gets +0.0. */
+ * A token whose K entries are all skipped gets +0.0. One persistent CTA per
+ * SM of the budget, the (token, column block) units split evenly over its
+ * warps; where dispatch would make a tail launch, combine hands the last
+ * 30 % of its units to one too (ep_combine_launches). */
 EP_API ep_status_t ep_combine(const uint16_t* expert_out, int64_t num_recv,
                        const int32_t* slot, const float* topk_w,
                        int64_t T, int64_t H, int K,

@@ -106,6 +106,18 @@ def test_dispatch_tail_percentage_round_trip(ep):
         ep.ep_set_dispatch_tail(before)
 
 
+def test_combine_tail_percentage_round_trip(ep):
+    before = ep.ep_get_combine_tail()
+    try:
+        assert before == 30
+        assert ep.ep_set_combine_tail(0) == 0 and ep.ep_get_combine_tail() == 0
+        assert ep.ep_set_combine_tail(91) == -1 and ep.ep_get_combine_tail() == 0
+    finally:
+        ep.ep_set_combine_tail(before)
+    assert ep.lib.ep_combine_launches(4096, 7166, 8, None) == -1    # H % 8 != 0
+    assert ep.lib.ep_combine_launches(0, 7168, 8, None) == 0
+
+
 def test_dispatch_launches_rejects_invalid_sizes(ep):
     # checked before the device is queried (no GPU needed)
     assert ep.lib.ep_dispatch_launches(4096, 7166, 8, None) == -1   # H % 8 != 0

@@ -841,10 +841,13 @@ def test_dispatch_launch_counts(ep):
     assert ep.ep_dispatch_launches(16384, 7168, 1) == 1    # K = 1
     assert ep.ep_layout_dispatch_launches(4096, 7168, 8, 256) == 3   # layout, ring, tail
     assert ep.ep_layout_dispatch_launches(128, 7168, 8, 256) == 2    # layout, dispatch
+    assert ep.ep_combine_launches(4096, 7168, 8) == 2                # persistent, tail
+    assert ep.ep_combine_launches(128, 7168, 8) == 1
     mode = ep.ep_get_launch_overlap()
     try:
         ep.ep_set_launch_overlap(2)
         assert ep.ep_dispatch_launches(4096, 7168, 8) == 1
+        assert ep.ep_combine_launches(4096, 7168, 8) == 1
     finally:
         ep.ep_set_launch_overlap(mode)
     try:
