@@ -712,6 +712,36 @@ def test_dispatch_tail_launch(ep, T, H, E, K, mask, routing, short):
             assert_parity(got, ref)
 
 
+@functools.lru_cache(maxsize=1)
+def _tail_share_case():
+    inp = _custom(16384, 7168, 256, 2, seed=911, mask=0.05, routing="zipf")
+    R_valid = int((inp.topk_idx >= 0).sum())
+    return inp, R_valid, oracle_path(inp, R_valid, 1.5)
+
+
+@pytest.mark.parametrize("percent", [1, 50, 90])
+def test_tail_shares_across_their_range(ep, percent):
+    """ep_set_dispatch_tail / ep_set_combine_tail move the split between the
+    persistent launch and the tail anywhere in 0-90 %: a tail of a few units,
+    one as large as the persistent part, and one nine times larger (the
+    persistent ring still keeps two units per warp at this size). Both calls
+    stay two launches and every output equals the oracle's, through both
+    call forms."""
+    inp, R_valid, ref = _tail_share_case()
+    T, H, K = inp.wl.T, inp.wl.H, inp.wl.K
+    ep.ep_set_num_sms(0)
+    try:
+        assert ep.ep_set_dispatch_tail(percent) == percent
+        assert ep.ep_set_combine_tail(percent) == percent
+        assert ep.ep_dispatch_launches(T, H, K) == 2
+        assert ep.ep_combine_launches(T, H, K) == 2
+        for fused in (False, True):
+            assert_parity(gpu_path(ep, inp, R_valid, ref.expert_out, num_sms=0, fused=fused), ref)
+    finally:
+        ep.ep_set_dispatch_tail(30)
+        ep.ep_set_combine_tail(30)
+
+
 @pytest.mark.parametrize("graph", [False, True])
 def test_combine_reads_the_rows_of_both_dispatch_launches(ep, graph):
     """Combine launched right after a two-launch dispatch (ring + tail, the
