@@ -685,12 +685,14 @@ def test_fused_one_launch_warps_split_by_the_id_count(ep, T, H, E, K, budget):
     (6144, 7176, 64, 3, 0.0, "uniform", 0),     # 14352-byte rows (a ragged last chunk)
     (2100, 6144, 32, 8, 0.25, "zipf", 0),       # just over the size limit (206 MB)
     (4096, 7168, 256, 8, 0.0, "uniform", 100),  # receive buffer 100 rows short
+    (2048, 7168, 64, 12, 0.1, "uniform", 0),    # K = 12: the generic combine path's tail
 ])
 def test_dispatch_tail_launch(ep, T, H, E, K, mask, routing, short):
     """At the full budget, with launches overlapping, a dispatch of at least
     192 MB of receive rows is two launches: a persistent ring over the first
     70 % of the (token, chunk) units, then a tail of small CTAs over the rest
-    that start on SMs whose ring CTA has finished. Every row must come out
+    that start on SMs whose ring CTA has finished; combine splits the same
+    way, K above 8 (its generic path) included. Every row must come out
     as the oracle's, through ep_dispatch and ep_layout_dispatch, with masked
     entries, skewed routing, a ragged last chunk, an odd number of tail
     units and rows beyond the receive buffer (reported, not written)."""
@@ -700,6 +702,7 @@ def test_dispatch_tail_launch(ep, T, H, E, K, mask, routing, short):
     num_recv = R_valid - short
     ep.ep_set_num_sms(0)
     assert ep.ep_dispatch_launches(T, H, K) == 2
+    assert ep.ep_combine_launches(T, H, K) == 2
     for fused in (False, True):
         got = gpu_path(ep, inp, num_recv, ref.expert_out, num_sms=0, fused=fused)
         if short:
